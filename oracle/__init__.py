@@ -1,0 +1,136 @@
+"""ctypes front end of the fp64 CPU oracle (``wq_oracle.cpp``).
+
+TEST INFRASTRUCTURE ONLY: imported by the tests, the smoke check and the
+benchmark's CPU-baseline leg, never by the library.  It shares no code with the
+CUDA path.  ``build()`` compiles the C++ source with g++ and OpenMP.
+
+All bf16 arrays cross this boundary as uint16 bit patterns.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from typing import Optional
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "wq_oracle.cpp")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lib: Optional[ctypes.CDLL] = None
+
+
+def build(force: bool = False) -> str:
+    """Compile liboracle.so (plain C++17, OpenMP, no FMA contraction)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        cmd = ["g++", "-std=c++17", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fopenmp",
+               "-shared", "-fPIC", "-o", tmp, _SRC]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load() -> ctypes.CDLL:
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(_LIB)
+        P = ctypes.c_void_p
+        i = ctypes.c_int
+        lib.wqo_words_per_row.argtypes = [i, i]
+        lib.wqo_words_per_row.restype = ctypes.c_long
+        lib.wqo_pack.argtypes = [P, P, i, i, i]
+        lib.wqo_unpack.argtypes = [P, P, i, i, i]
+        lib.wqo_dequant_f64.argtypes = [P, P, P, P, i, i, i, i]
+        lib.wqo_dequant_bf16.argtypes = [P, P, P, P, i, i, i, i]
+        lib.wqo_bf16_rne.argtypes = [ctypes.c_double]
+        lib.wqo_bf16_rne.restype = ctypes.c_uint16
+        lib.wqo_gemm_f64.argtypes = [P, P, P, P, P, i, i, i, i, i, i]
+        lib.wqo_max_threads.argtypes = [i]
+        for fn in (lib.wqo_pack, lib.wqo_unpack, lib.wqo_dequant_f64, lib.wqo_dequant_bf16,
+                   lib.wqo_gemm_f64, lib.wqo_max_threads):
+            fn.restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def _ptr(a: np.ndarray):
+    assert a.flags["C_CONTIGUOUS"]
+    return ctypes.c_void_p(a.ctypes.data)
+
+
+def words_per_row(K: int, bits: int) -> int:
+    return int(_load().wqo_words_per_row(K, bits))
+
+
+def pack(q: np.ndarray, bits: int) -> np.ndarray:
+    q = np.ascontiguousarray(q, dtype=np.uint8)
+    N, K = q.shape
+    out = np.zeros((N, words_per_row(K, bits)), dtype=np.uint32)
+    if _load().wqo_pack(_ptr(q), _ptr(out), N, K, bits):
+        raise ValueError("oracle pack: bad arguments")
+    return out
+
+
+def unpack(wq: np.ndarray, K: int, bits: int) -> np.ndarray:
+    wq = np.ascontiguousarray(wq, dtype=np.uint32)
+    N = wq.shape[0]
+    out = np.zeros((N, K), dtype=np.uint8)
+    if _load().wqo_unpack(_ptr(wq), _ptr(out), N, K, bits):
+        raise ValueError("oracle unpack: bad arguments")
+    return out
+
+
+def dequant_f64(wq, s, z, K: int, group: int, bits: int) -> np.ndarray:
+    wq = np.ascontiguousarray(wq, dtype=np.uint32)
+    s = np.ascontiguousarray(s, dtype=np.uint16)
+    z = np.ascontiguousarray(z, dtype=np.uint8)
+    N = wq.shape[0]
+    out = np.zeros((N, K), dtype=np.float64)
+    if _load().wqo_dequant_f64(_ptr(wq), _ptr(s), _ptr(z), _ptr(out), N, K, group, bits):
+        raise ValueError("oracle dequant: bad arguments")
+    return out
+
+
+def dequant_bf16(wq, s, z, K: int, group: int, bits: int) -> np.ndarray:
+    wq = np.ascontiguousarray(wq, dtype=np.uint32)
+    s = np.ascontiguousarray(s, dtype=np.uint16)
+    z = np.ascontiguousarray(z, dtype=np.uint8)
+    N = wq.shape[0]
+    out = np.zeros((N, K), dtype=np.uint16)
+    if _load().wqo_dequant_bf16(_ptr(wq), _ptr(s), _ptr(z), _ptr(out), N, K, group, bits):
+        raise ValueError("oracle dequant: bad arguments")
+    return out
+
+
+def bf16_rne(v: float) -> int:
+    return int(_load().wqo_bf16_rne(float(v)))
+
+
+def gemm_f64(x, wq, s, z, K: int, group: int, bits: int, threads: int = 0) -> np.ndarray:
+    """Y[M][N] (float64) for x [M][K] bf16 bits and packed rows wq [N][W]."""
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    wq = np.ascontiguousarray(wq, dtype=np.uint32)
+    s = np.ascontiguousarray(s, dtype=np.uint16)
+    z = np.ascontiguousarray(z, dtype=np.uint8)
+    M, N = x.shape[0], wq.shape[0]
+    y = np.zeros((M, N), dtype=np.float64)
+    if _load().wqo_gemm_f64(_ptr(x), _ptr(wq), _ptr(s), _ptr(z), _ptr(y), M, N, K, group, bits,
+                            threads):
+        raise ValueError("oracle gemm: bad arguments")
+    return y
+
+
+def max_threads(threads: int = 0) -> int:
+    return int(_load().wqo_max_threads(threads))
+
+
+def step_floor_seconds(weight_bytes: float, bandwidth_bytes_per_s: float) -> float:
+    """Closed-form decode-step floor when every weight byte is read once per step.
+
+    OpenJet news page, paragraph "并行解码的原理": the step is bound by reading all
+    weights from memory once, so its time is at least bytes / bandwidth.
+    """
+    return weight_bytes / bandwidth_bytes_per_s
