@@ -1,0 +1,169 @@
+/*
+ * libwq — weight-only low-bit skinny GEMM for the decode step (sm_103a).
+ *
+ * The operation (OpenJet news page "单张 RTX 3090 跑 4 个编码 agent", paragraph
+ * "并行解码的原理"): in a decode step every packed low-bit weight is streamed
+ * from memory once and, while on chip, multiplied against all stacked rows
+ * (each active agent's next token plus its draft tokens):
+ *
+ *     Y[M][N] = X[M][K] . dequant(Wq)[N][K]^T,   M = 1..16
+ *     dequant(Wq)[n][k] = (q[n][k] - z[n][k/G]) * s[n][k/G]
+ *
+ * with 2/3/4-bit codes chosen per layer and repacked at load time (Agens
+ * Engine page, section "功能": 混合 2/3/4-bit 权重, 加载时重新打包) and a group
+ * size of 128 along K for the 4-bit format (Agens SGLang README, "Quick
+ * start": W4A16, group size 128).
+ *
+ * Data layout (all row-major, all pointers are DEVICE pointers owned by the
+ * caller unless stated otherwise):
+ *   q       uint8  [N][K]        unpacked codes; only the low `bits` bits are used
+ *   wq      uint32 [N][W]        packed codes, W = wq_packed_words_per_row(K, bits):
+ *                                code k of a row lives in word k / vpw at bits
+ *                                [bits*(k % vpw), bits*(k % vpw) + bits), least
+ *                                significant first; vpw = 8 (4-bit), 10 (3-bit,
+ *                                bits 30..31 zero), 16 (2-bit); words run along K
+ *                                across group boundaries; unused slots and the
+ *                                padding words that round a row up to a multiple
+ *                                of 4 words (16 bytes) are zero
+ *   scales  bf16   [N][K/G]      per-group scale s (bf16 bit patterns, uint16)
+ *   zeros   uint8  [N][K/G]      per-group zero point z
+ *   x       bf16   [M][K]        activations (bf16 bit patterns)
+ *   y       fp32   [M][N]        output
+ *   w       bf16   [N][K]        dequantised weights (wq_dequant output)
+ *
+ * Arguments: bits in {2, 3, 4}; group in {32, 64, 128}; K % group == 0;
+ * 0 <= M <= 16; N, K >= 0.  x and wq must be 16-byte aligned, y 4-byte
+ * aligned, scales 2-byte aligned.  Streams are passed as `void*` holding a
+ * cudaStream_t (NULL = the legacy default stream).  Every call is
+ * asynchronous on its stream and returns a status; kernels never trap:
+ * invalid arguments are rejected on the host before anything is launched.
+ * Calls on distinct streams are thread-safe except where a workspace is
+ * shared (see wq_gemm).
+ */
+#ifndef WQ_H
+#define WQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    WQ_OK = 0,
+    WQ_ERR_INVALID_ARG = 1, /* null pointer, bad size/bits/group, misalignment, small workspace */
+    WQ_ERR_UNSUPPORTED = 2, /* device is not sm_103, or a feature the build lacks */
+    WQ_ERR_CUDA = 3,        /* a CUDA runtime call failed; see wq_last_cuda_error() */
+    WQ_ERR_TIMEOUT = 4      /* a kernel gave up a bounded wait (wq_check_workspace) */
+} wq_status_t;
+
+/* ABI version of this header (major * 100 + minor). */
+int wq_abi_version(void);
+
+/* Static description of a status code. */
+const char* wq_status_string(wq_status_t status);
+
+/* cudaError_t of the last failing CUDA call made by this thread inside libwq. */
+int wq_last_cuda_error(void);
+
+/* Words per packed row: ceil(K / vpw) rounded up to a multiple of 4, or -1 for
+ * bad arguments.  Layout: see the header comment. */
+long wq_packed_words_per_row(int K, int bits);
+
+/*
+ * wq_pack — repack unpacked codes q[N][K] into wq[N][W] (load time; Agens
+ * Engine page, section "功能": 加载时重新打包).  Bit-exact; the padding words of
+ * every row are written as zero.  q and wq must not overlap.
+ */
+wq_status_t wq_pack(const uint8_t* q, uint32_t* wq, int N, int K, int bits, void* stream);
+
+/* wq_unpack — inverse of wq_pack (a test aid): wq[N][W] -> q[N][K]. */
+wq_status_t wq_unpack(const uint32_t* wq, uint8_t* q, int N, int K, int bits, void* stream);
+
+/*
+ * wq_dequant — materialise bf16 weights w[N][K] = RNE_bf16((q - z) * s), the
+ * exact product rounded once to nearest even.  Group-wise scale and zero point
+ * along K: Agens SGLang README, "Quick start" (W4A16, group size 128).
+ * Bit-exact against the plain definition (Agens SGLang README, "Server
+ * environment variables": fast paths are bit-exact with the plain path).
+ */
+wq_status_t wq_dequant(const uint32_t* wq, const uint16_t* scales, const uint8_t* zeros,
+                       uint16_t* w, int N, int K, int group, int bits, void* stream);
+
+/*
+ * Workspace for wq_gemm on the CURRENT device: split-K partial sums and
+ * per-tile arrival counters (it depends on N, K, bits and the SM count, never
+ * on M).  Returns 0 for bad arguments.
+ */
+size_t wq_workspace_bytes(int M, int N, int K, int group, int bits);
+
+/* Zero a caller-owned workspace (required once before its first use; every
+ * wq_gemm call leaves it zeroed again). */
+wq_status_t wq_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * wq_gemm — Y[M][N] = X[M][K] . dequant(Wq)[N][K]^T with fp32 accumulation
+ * (OpenJet news page, paragraph "并行解码的原理": one pass over the packed
+ * weights against all stacked rows, on tensor cores).
+ *
+ * Numerics: (q - z) enters the tensor-core product exactly; the bf16 scale is
+ * applied per group in fp32; Y is fp32.  The reduction order of every output
+ * depends only on (N, K, group, bits, SM count), never on M or on the other
+ * rows of X, so a row's result is bit-identical whether it is computed alone
+ * or stacked with other rows (OpenJet news page, "新提示不会让所有人停摆":
+ * results bit-identical to processing alone), and repeated calls are
+ * bit-identical.
+ *
+ * workspace: device buffer of at least wq_workspace_bytes(...) bytes, zeroed
+ * once by wq_workspace_init; calls that share one workspace must be ordered
+ * (same stream).  workspace == NULL uses a library-owned buffer per device,
+ * allocated (and zeroed) on the first call on that device — make that first
+ * call outside stream capture; the library buffer must not be used by calls
+ * that overlap on the GPU.
+ */
+wq_status_t wq_gemm(const uint16_t* x, const uint32_t* wq, const uint16_t* scales,
+                    const uint8_t* zeros, float* y, int M, int N, int K, int group, int bits,
+                    void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Read back the kernel error word of a workspace (NULL = the library buffer
+ * of the current device) after synchronising `stream`: WQ_OK, or
+ * WQ_ERR_TIMEOUT if a kernel abandoned a bounded wait since the last check.
+ * Clears the word.
+ */
+wq_status_t wq_check_workspace(void* workspace, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Decode-step driver: a whole layer stack's projections back to back on one
+ * stream (OpenJet news page, paragraph "并行解码的原理": every projection of
+ * every layer streams its weights once per step).
+ * ------------------------------------------------------------------------ */
+typedef struct wq_proj_desc {
+    const uint16_t* x;       /* [M][K] bf16 */
+    const uint32_t* wq;      /* [N][W] */
+    const uint16_t* scales;  /* [N][K/G] bf16 */
+    const uint8_t* zeros;    /* [N][K/G] */
+    float* y;                /* [M][N] fp32 */
+    int M, N, K, group, bits;
+} wq_proj_desc_t;
+
+/* Run `count` projections in order on `stream` (one wq_gemm each). */
+wq_status_t wq_step_run(const wq_proj_desc_t* projs, int count, void* workspace,
+                        size_t workspace_bytes, void* stream);
+
+typedef struct wq_step_graph* wq_step_graph_t;
+
+/* Capture the same launch sequence once into a CUDA graph (no host work per
+ * replay).  The descriptors' pointers are baked in: the buffers must stay
+ * alive and in place while the graph exists.  `workspace` must be non-NULL. */
+wq_status_t wq_step_graph_create(const wq_proj_desc_t* projs, int count, void* workspace,
+                                 size_t workspace_bytes, void* stream, wq_step_graph_t* out);
+wq_status_t wq_step_graph_launch(wq_step_graph_t graph, void* stream);
+void wq_step_graph_destroy(wq_step_graph_t graph);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* WQ_H */

@@ -1,0 +1,89 @@
+"""CPU-side checks of the C ABI: the library loads, exports every declared
+symbol, and rejects bad arguments on the host before touching a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import __graft_entry__
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def wq():
+    __graft_entry__.build()
+    import weight_only_bit_wq_gb300 as m
+    return m
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "wq.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(wq_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(wq):
+    names = _declared()
+    assert "wq_gemm" in names and "wq_pack" in names and "wq_dequant" in names
+    lib = ctypes.CDLL(wq.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(wq.EXPORTED) <= set(names)
+
+
+def test_abi_version_and_words(wq):
+    assert wq.abi_version() == 100
+    assert wq.wq_packed_words_per_row(17408, 3) == 1744
+    assert wq.wq_packed_words_per_row(5120, 4) == 640
+    assert wq.wq_packed_words_per_row(17408, 2) == 1088
+    assert wq.wq_packed_words_per_row(10, 5) == -1
+
+
+def _gemm(lib, M=4, N=8, K=128, group=128, bits=4, x=16, w=16, s=16, z=16, y=16):
+    P = ctypes.c_void_p
+    return lib.wq_gemm(P(x), P(w), P(s), P(z), P(y), M, N, K, group, bits, P(0), 0, P(0))
+
+
+def test_gemm_rejects_bad_arguments_on_host(wq):
+    lib = wq._lib()
+    bad = wq.WQ_ERR_INVALID_ARG
+    assert _gemm(lib, bits=5) == bad
+    assert _gemm(lib, bits=1) == bad
+    assert _gemm(lib, group=96) == bad
+    assert _gemm(lib, K=100, group=32) == bad     # K % group != 0
+    assert _gemm(lib, M=17) == bad
+    assert _gemm(lib, M=-1) == bad
+    assert _gemm(lib, N=-3) == bad
+    assert _gemm(lib, y=0) == bad                 # null output
+    assert _gemm(lib, y=2) == bad                 # misaligned output
+
+
+def test_empty_problems_are_no_ops(wq):
+    lib = wq._lib()
+    assert _gemm(lib, M=0, x=0, w=0, s=0, z=0, y=0) == wq.WQ_OK
+    assert _gemm(lib, N=0, x=0, w=0, s=0, z=0, y=0) == wq.WQ_OK
+    P = ctypes.c_void_p
+    assert lib.wq_pack(P(0), P(0), 0, 64, 4, P(0)) == wq.WQ_OK
+    assert lib.wq_unpack(P(0), P(0), 5, 0, 4, P(0)) == wq.WQ_OK
+    assert lib.wq_dequant(P(0), P(0), P(0), P(0), 0, 128, 128, 4, P(0)) == wq.WQ_OK
+
+
+def test_elementwise_rejects_bad_arguments(wq):
+    lib = wq._lib()
+    P = ctypes.c_void_p
+    bad = wq.WQ_ERR_INVALID_ARG
+    assert lib.wq_pack(P(16), P(16), 4, 64, 5, P(0)) == bad
+    assert lib.wq_pack(P(16), P(0), 4, 64, 4, P(0)) == bad
+    assert lib.wq_pack(P(16), P(18), 4, 64, 4, P(0)) == bad
+    assert lib.wq_dequant(P(16), P(16), P(16), P(16), 4, 100, 32, 4, P(0)) == bad
+    assert lib.wq_dequant(P(16), P(0), P(16), P(16), 4, 128, 32, 4, P(0)) == bad
+    assert lib.wq_step_run(P(0), 3, P(0), 0, P(0)) == bad
+    assert lib.wq_step_graph_create(P(0), 1, P(0), 0, P(0), P(0)) == bad
+
+
+@pytest.mark.parametrize("U,P", [(1, 1), (7, 7), (10, 4), (5440, 152), (160, 64), (32, 32),
+                                 (1000003, 152), (272 * 20, 152), (17, 5)])
+def test_stream_k_schedule_partitions_units(wq, U, P):
+    assert wq._lib().wq_internal_schedule_check(U, P) == 0

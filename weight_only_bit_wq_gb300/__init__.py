@@ -1,0 +1,211 @@
+"""Python binding of libwq (ctypes; argument marshalling only).
+
+Every entry point has the name of the C function it calls (include/wq.h) and
+passes torch tensors' device pointers plus the current CUDA stream.  All
+arithmetic runs in libwq's CUDA kernels; there is no fallback: if libwq.so is
+missing or a call fails, an exception is raised.
+
+bf16 tensors may be given as torch.bfloat16 or as their int16/uint16 bit
+patterns; packed words are held in torch.int32 tensors (bit patterns of the
+uint32 words).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import List, Optional, Sequence
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libwq.so")
+
+WQ_OK, WQ_ERR_INVALID_ARG, WQ_ERR_UNSUPPORTED, WQ_ERR_CUDA, WQ_ERR_TIMEOUT = range(5)
+
+EXPORTED = ("wq_abi_version", "wq_status_string", "wq_last_cuda_error", "wq_packed_words_per_row",
+            "wq_pack", "wq_unpack", "wq_dequant", "wq_workspace_bytes", "wq_workspace_init",
+            "wq_gemm", "wq_check_workspace", "wq_step_run", "wq_step_graph_create",
+            "wq_step_graph_launch", "wq_step_graph_destroy")
+
+
+class WQError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        lib = _lib()
+        msg = lib.wq_status_string(status).decode()
+        if status == WQ_ERR_CUDA:
+            msg += f" (cudaError {lib.wq_last_cuda_error()})"
+        super().__init__(f"{where}: {msg}")
+
+
+class ProjDesc(ctypes.Structure):
+    _fields_ = [("x", ctypes.c_void_p), ("wq", ctypes.c_void_p), ("scales", ctypes.c_void_p),
+                ("zeros", ctypes.c_void_p), ("y", ctypes.c_void_p), ("M", ctypes.c_int),
+                ("N", ctypes.c_int), ("K", ctypes.c_int), ("group", ctypes.c_int),
+                ("bits", ctypes.c_int)]
+
+
+_LIB: Optional[ctypes.CDLL] = None
+
+
+def _lib() -> ctypes.CDLL:
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libwq.so is not built ({LIB_PATH}); run weight_only_bit_wq_gb300.build.build()")
+        lib = ctypes.CDLL(LIB_PATH)
+        P, I, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+        sig = {
+            "wq_abi_version": ([], I),
+            "wq_status_string": ([I], ctypes.c_char_p),
+            "wq_last_cuda_error": ([], I),
+            "wq_packed_words_per_row": ([I, I], ctypes.c_long),
+            "wq_pack": ([P, P, I, I, I, P], I),
+            "wq_unpack": ([P, P, I, I, I, P], I),
+            "wq_dequant": ([P, P, P, P, I, I, I, I, P], I),
+            "wq_workspace_bytes": ([I, I, I, I, I], S),
+            "wq_workspace_init": ([P, S, P], I),
+            "wq_gemm": ([P, P, P, P, P, I, I, I, I, I, P, S, P], I),
+            "wq_check_workspace": ([P, P], I),
+            "wq_step_run": ([P, I, P, S, P], I),
+            "wq_step_graph_create": ([P, I, P, S, P, P], I),
+            "wq_step_graph_launch": ([P, P], I),
+            "wq_step_graph_destroy": ([P], None),
+            "wq_internal_schedule_check": ([ctypes.c_longlong, I], I),
+        }
+        for name, (args, res) in sig.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = res
+        _LIB = lib
+    return _LIB
+
+
+def _check(status: int, where: str) -> None:
+    if status != WQ_OK:
+        raise WQError(status, where)
+
+
+def _stream(stream=None) -> ctypes.c_void_p:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t: Optional[torch.Tensor]) -> ctypes.c_void_p:
+    if t is None:
+        return ctypes.c_void_p(0)
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def abi_version() -> int:
+    return int(_lib().wq_abi_version())
+
+
+def wq_packed_words_per_row(K: int, bits: int) -> int:
+    return int(_lib().wq_packed_words_per_row(K, bits))
+
+
+def wq_pack(q: torch.Tensor, bits: int, out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """uint8 codes [N][K] -> packed words [N][W] (int32 bit patterns)."""
+    N, K = q.shape
+    W = wq_packed_words_per_row(K, bits)
+    if out is None:
+        out = torch.empty((N, max(W, 0)), dtype=torch.int32, device=q.device)
+    _check(_lib().wq_pack(_ptr(q), _ptr(out), N, K, bits, _stream(stream)), "wq_pack")
+    return out
+
+
+def wq_unpack(wq: torch.Tensor, K: int, bits: int, out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    N = wq.shape[0]
+    if out is None:
+        out = torch.empty((N, K), dtype=torch.uint8, device=wq.device)
+    _check(_lib().wq_unpack(_ptr(wq), _ptr(out), N, K, bits, _stream(stream)), "wq_unpack")
+    return out
+
+
+def wq_dequant(wq, scales, zeros, K: int, group: int, bits: int, out=None, stream=None) -> torch.Tensor:
+    """bf16 weights [N][K] = RNE((q - z) * s)."""
+    N = wq.shape[0]
+    if out is None:
+        out = torch.empty((N, K), dtype=torch.bfloat16, device=wq.device)
+    _check(_lib().wq_dequant(_ptr(wq), _ptr(scales), _ptr(zeros), _ptr(out), N, K, group, bits,
+                             _stream(stream)), "wq_dequant")
+    return out
+
+
+def wq_workspace_bytes(M: int, N: int, K: int, group: int, bits: int) -> int:
+    return int(_lib().wq_workspace_bytes(M, N, K, group, bits))
+
+
+def wq_workspace_init(ws: torch.Tensor, stream=None) -> torch.Tensor:
+    _check(_lib().wq_workspace_init(_ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
+           "wq_workspace_init")
+    return ws
+
+
+def new_workspace(M: int, N: int, K: int, group: int, bits: int, device="cuda") -> torch.Tensor:
+    """A zeroed workspace for wq_gemm calls of this shape (or smaller)."""
+    nbytes = wq_workspace_bytes(M, N, K, group, bits)
+    if nbytes == 0:
+        raise WQError(WQ_ERR_INVALID_ARG, "wq_workspace_bytes")
+    return wq_workspace_init(torch.empty(nbytes, dtype=torch.uint8, device=device))
+
+
+def wq_gemm(x, wq, scales, zeros, N: int, group: int, bits: int, out=None, workspace=None,
+            stream=None) -> torch.Tensor:
+    """Y[M][N] (fp32) = X[M][K] . dequant(Wq)[N][K]^T."""
+    M, K = x.shape
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(_lib().wq_gemm(_ptr(x), _ptr(wq), _ptr(scales), _ptr(zeros), _ptr(out), M, N, K, group,
+                          bits, _ptr(workspace), nbytes, _stream(stream)), "wq_gemm")
+    return out
+
+
+def wq_check_workspace(workspace=None, stream=None) -> None:
+    _check(_lib().wq_check_workspace(_ptr(workspace), _stream(stream)), "wq_check_workspace")
+
+
+def make_descs(projs: Sequence[dict]) -> ctypes.Array:
+    """Descriptor array from dicts with keys x, wq, scales, zeros, y, M, N, K, group, bits."""
+    arr = (ProjDesc * len(projs))()
+    for i, p in enumerate(projs):
+        arr[i] = ProjDesc(p["x"].data_ptr(), p["wq"].data_ptr(), p["scales"].data_ptr(),
+                          p["zeros"].data_ptr(), p["y"].data_ptr(), p["M"], p["N"], p["K"],
+                          p["group"], p["bits"])
+    return arr
+
+
+def wq_step_run(descs: ctypes.Array, workspace: torch.Tensor, stream=None) -> None:
+    _check(_lib().wq_step_run(ctypes.cast(descs, ctypes.c_void_p), len(descs), _ptr(workspace),
+                              workspace.numel(), _stream(stream)), "wq_step_run")
+
+
+class StepGraph:
+    """A captured decode step (wq_step_graph_create / _launch / _destroy)."""
+
+    def __init__(self, descs: ctypes.Array, workspace: torch.Tensor, stream=None):
+        self._descs = descs
+        self._ws = workspace
+        h = ctypes.c_void_p(0)
+        _check(_lib().wq_step_graph_create(ctypes.cast(descs, ctypes.c_void_p), len(descs),
+                                           _ptr(workspace), workspace.numel(), _stream(stream),
+                                           ctypes.byref(h)), "wq_step_graph_create")
+        self._h = h
+
+    def launch(self, stream=None) -> None:
+        _check(_lib().wq_step_graph_launch(self._h, _stream(stream)), "wq_step_graph_launch")
+
+    def close(self) -> None:
+        if self._h:
+            _lib().wq_step_graph_destroy(self._h)
+            self._h = ctypes.c_void_p(0)
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

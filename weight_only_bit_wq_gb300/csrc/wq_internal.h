@@ -1,0 +1,58 @@
+// Host-side declarations shared by the library's translation units.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace wq {
+
+constexpr int kConsumerWarps = 8;
+constexpr int kThreads = 32 * (kConsumerWarps + 1);  // + one TMA producer warp
+constexpr int kBN = 16 * kConsumerWarps;             // weight rows per tile
+constexpr int kWordsPerStage = 32;                   // packed words per row per stage (128 B)
+constexpr int kMaxCols = 16;                         // max stacked rows M
+constexpr int kMaxSplit = 8;                         // max CTAs sharing one tile
+constexpr size_t kWsHeader = 256;                    // error word + padding
+
+// Values per packed word and per stage.
+constexpr int values_per_word(int bits) { return bits == 4 ? 8 : bits == 3 ? 10 : 16; }
+constexpr int stage_values(int bits) { return kWordsPerStage * values_per_word(bits); }
+
+struct GemmArgs {
+    const uint16_t* scales;
+    const uint8_t* zeros;
+    float* y;
+    float* partials;  // [2 * P][kMaxCols][kBN]
+    int* counters;    // [T]
+    int* err;         // kernel error word
+    int M, N, K, ng;
+    int T, I;         // tiles, k-stages per tile
+    long long U;      // T * I work units
+    int P;            // CTAs
+};
+
+// Static stream-K schedule: CTA b owns units [unit_begin(b), unit_begin(b+1)).
+inline long long unit_begin(long long U, int P, int b) { return U * b / P; }
+
+// Grid size from (N, K, bits) and the SM count only (never from M).
+int choose_grid(int T, int I, int sm_count);
+
+// Per-bit-width launchers (one translation unit each).
+cudaError_t launch_gemm_b4(int group, int nt, const CUtensorMap& tmW, const CUtensorMap& tmX,
+                           const GemmArgs& a, cudaStream_t s);
+cudaError_t launch_gemm_b2(int group, int nt, const CUtensorMap& tmW, const CUtensorMap& tmX,
+                           const GemmArgs& a, cudaStream_t s);
+cudaError_t launch_gemm_b3(int group, int nt, const CUtensorMap& tmW, const CUtensorMap& tmX,
+                           const GemmArgs& a, cudaStream_t s);
+
+// Elementwise kernels.
+cudaError_t launch_pack(const uint8_t* q, uint32_t* wq, int N, int K, int bits, int W,
+                        int sm_count, cudaStream_t s);
+cudaError_t launch_unpack(const uint32_t* wq, uint8_t* q, int N, int K, int bits, int W,
+                          int sm_count, cudaStream_t s);
+cudaError_t launch_dequant(const uint32_t* wq, const uint16_t* scales, const uint8_t* zeros,
+                           uint16_t* w, int N, int K, int group, int bits, int W, int sm_count,
+                           cudaStream_t s);
+
+}  // namespace wq
