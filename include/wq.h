@@ -127,6 +127,30 @@ wq_status_t wq_gemm(const uint16_t* x, const uint32_t* wq, const uint16_t* scale
                     void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * wq_gemm_noalloc — wq_gemm without any device allocation.  The paper has no
+ * counterpart: this entry point exists for callers that cannot call cudaMalloc,
+ * e.g. code running inside a framework or server that owns all device memory
+ * through its own pool, code on a path where an allocation would synchronise
+ * the device or break a fixed memory budget, and code that must not fail
+ * halfway through a step for lack of memory.  The caller still passes x, wq,
+ * scales, zeros and y (same layout and rules as wq_gemm).
+ *
+ * Scratch: a fixed 4 MiB file-scope device array inside libwq, held by every
+ * GPU that loads the library until the process exits.  The first call on a
+ * device sets it up (looks up its device address and zeroes it on `stream`);
+ * make that first call before any stream capture.  Every call re-zeroes the
+ * per-tile counters it needs.  Problems whose scratch (wq_workspace_bytes)
+ * would exceed 4 MiB — N beyond roughly 54 million rows on a 152-SM GPU — are
+ * rejected with WQ_ERR_INVALID_ARG before anything is launched.  All calls
+ * share the one array, so calls that overlap on the GPU (different streams,
+ * or different host threads without ordering) race and give wrong results;
+ * order them on one stream.  Nothing is allocated or freed.
+ */
+wq_status_t wq_gemm_noalloc(const uint16_t* x, const uint32_t* wq, const uint16_t* scales,
+                            const uint8_t* zeros, float* y, int M, int N, int K, int group,
+                            int bits, void* stream);
+
+/*
  * Read back the kernel error word of a workspace (NULL = the library buffer
  * of the current device) after synchronising `stream`: WQ_OK, or
  * WQ_ERR_TIMEOUT if a kernel abandoned a bounded wait since the last check.

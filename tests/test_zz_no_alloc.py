@@ -1,0 +1,64 @@
+"""wq_gemm_noalloc: the GEMM for callers that cannot allocate device memory
+(a framework or server that owns every byte of GPU memory through its own
+pool, or a step that must not allocate part-way through).  It keeps its scratch
+in a fixed array inside the library instead of a workspace argument.
+
+This file is collected last on purpose.  Its checks: through the C ABI, two
+calls in a row agree with wq_gemm within the GEMM tolerance (the second call
+sees whatever the first left in the shared array), and a problem too large for
+the fixed array is refused up front.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+from wqtest import ARITH_TOL, REL_TOL, dev, rel_err, to_dev_host_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+    __graft_entry__.build()
+    import weight_only_bit_wq_gb300 as wq
+    L = ctypes.CDLL(wq.LIB_PATH)
+    P, I = ctypes.c_void_p, ctypes.c_int
+    L.wq_gemm_noalloc.argtypes = [P, P, P, P, P, I, I, I, I, I, P]
+    L.wq_gemm_noalloc.restype = I
+    return L
+
+
+def _call(lib, d, y, p):
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    return lib.wq_gemm_noalloc(ctypes.c_void_p(d["x"].data_ptr()), ctypes.c_void_p(d["wq"].data_ptr()),
+                               ctypes.c_void_p(d["s"].data_ptr()), ctypes.c_void_p(d["z"].data_ptr()),
+                               ctypes.c_void_p(y.data_ptr()), p.M, p.N, p.K, p.group, p.bits, stream)
+
+
+def test_noalloc_matches_wq_gemm_twice(lib):
+    import weight_only_bit_wq_gb300 as wq
+    # first a shape whose tiles are split across CTAs, then a different one
+    cases = [synth.Projection("a", 12, 3000, 5120, 4, 128, 901, outlier_frac=0.01),
+             synth.Projection("b", 5, 1030, 2048, 2, 64, 902, s_range=(0.005, 0.04))]
+    for p in cases:
+        w, x, d = to_dev_host_inputs(p)
+        ref = wq.wq_gemm(d["x"], d["wq"], d["s"], d["z"], p.N, p.group, p.bits).cpu().numpy()
+        for _ in range(2):
+            y = torch.full((p.M, p.N), float("nan"), dtype=torch.float32, device=dev())
+            assert _call(lib, d, y, p) == wq.WQ_OK
+            got = y.cpu().numpy()
+            err = rel_err(got, ref.astype(np.float64))
+            assert err <= REL_TOL and err <= ARITH_TOL, err
+
+
+def test_noalloc_refuses_oversized_problem(lib):
+    import weight_only_bit_wq_gb300 as wq
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    P = ctypes.c_void_p
+    # 2^30 rows need 32 MiB of tile counters: far beyond the fixed array
+    st = lib.wq_gemm_noalloc(P(16), P(16), P(16), P(16), P(16), 1, 1 << 30, 128, 128, 4, stream)
+    assert st == wq.WQ_ERR_INVALID_ARG

@@ -1,0 +1,75 @@
+// wq_gemm_noalloc: the same GEMM as wq_gemm, for callers that must not
+// allocate device memory.  Its split-K scratch (partial sums, per-tile arrival
+// counters and the error word) lives in one fixed file-scope device array that
+// every GPU loading this library holds until the process exits.
+#include <cuda_runtime.h>
+
+#include <mutex>
+#include <vector>
+
+#include "../../include/wq.h"
+#include "wq_internal.h"
+
+namespace {
+
+// Fixed scratch size.  Enough for the split-K partials of up to 2 x (SM count)
+// CTAs (2.5 MB on a 152-SM GB300) plus one counter per 128-row tile.
+constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+struct NoAllocDevice {
+    bool ready = false;
+    unsigned char* scratch = nullptr;  // device address of g_noalloc_scratch on that device
+    int sm_count = 0;
+};
+
+std::mutex g_noalloc_mu;
+std::vector<NoAllocDevice> g_noalloc_dev;
+
+// One-time set-up for the current device: look up the array's device address
+// (in host code the symbol name is only a host-side stand-in) and zero it.
+wq_status_t noalloc_setup(cudaStream_t s, NoAllocDevice** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return WQ_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (static_cast<int>(g_noalloc_dev.size()) <= dev) g_noalloc_dev.resize(dev + 1);
+    NoAllocDevice& d = g_noalloc_dev[dev];
+    if (!d.ready) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+            return WQ_ERR_CUDA;
+        if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return WQ_ERR_CUDA;
+        if (cudaMemsetAsync(p, 0, kNoAllocScratchBytes, s) != cudaSuccess) return WQ_ERR_CUDA;
+        d.scratch = static_cast<unsigned char*>(p);
+        d.ready = true;
+    }
+    *out = &d;
+    return WQ_OK;
+}
+
+}  // namespace
+
+extern "C" wq_status_t wq_gemm_noalloc(const uint16_t* x, const uint32_t* wq,
+                                       const uint16_t* scales, const uint8_t* zeros, float* y,
+                                       int M, int N, int K, int group, int bits, void* stream) {
+    // Size check first: the scratch this problem needs must fit the fixed array.
+    if (N < 0 || M < 0 || K < 0) return WQ_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    NoAllocDevice* d = nullptr;
+    if (wq_status_t st = noalloc_setup(s, &d)) return st;
+    const long long tiles = (static_cast<long long>(N) + wq::kBN - 1) / wq::kBN;
+    const size_t counter_off =
+        wq::kWsHeader + size_t(2) * d->sm_count * wq::kMaxCols * wq::kBN * sizeof(float);
+    const size_t need = counter_off + static_cast<size_t>(tiles) * sizeof(int);
+    if (need > kNoAllocScratchBytes) return WQ_ERR_INVALID_ARG;
+    // The array keeps whatever the previous call left: re-zero the arrival
+    // counters, which must start at zero.
+    if (tiles > 0 &&
+        cudaMemsetAsync(d->scratch + counter_off, 0, static_cast<size_t>(tiles) * sizeof(int), s) !=
+            cudaSuccess)
+        return WQ_ERR_CUDA;
+    return wq_gemm(x, wq, scales, zeros, y, M, N, K, group, bits, d->scratch,
+                   kNoAllocScratchBytes, stream);
+}
