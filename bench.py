@@ -50,6 +50,9 @@ def parse_args(argv=None):
     ap.add_argument("--no-configs", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU oracle sample budget")
     ap.add_argument("--layers", type=int, default=64)
+    ap.add_argument("--profile-config", default=None,
+                    help="only run CALLS single wq_gemm calls of this config (for ncu captures)")
+    ap.add_argument("--calls", type=int, default=3)
     return ap.parse_args(argv)
 
 
@@ -554,8 +557,38 @@ def main_reference(args):
     return 0
 
 
+def main_profile(args):
+    """A few plain calls of one seeded config on cuda:0 (small enough for ncu)."""
+    import numpy as np
+    import torch
+
+    import __graft_entry__
+    import synth
+    import weight_only_bit_wq_gb300 as wq
+
+    __graft_entry__.build()
+    device = torch.device("cuda", 0)
+    p = synth.CONFIGS[args.profile_config]
+    if args.m != HEADLINE_M:
+        p = p.with_m(args.m) if p.x_row_seeds is None or args.m <= len(p.x_row_seeds) else p
+    q, s, z = synth.gen_weights_torch(p, device)
+    wqw = wq.wq_pack(q, p.bits)
+    del q
+    x = torch.from_numpy(synth.gen_x(p).view(np.int16)).to(device)
+    ws = wq.new_workspace(p.M, p.N, p.K, p.group, p.bits, device=device)
+    y = torch.empty((p.M, p.N), dtype=torch.float32, device=device)
+    for _ in range(args.calls):
+        wq.wq_gemm(x, wqw, s, z, p.N, p.group, p.bits, out=y, workspace=ws)
+    torch.cuda.synchronize()
+    wq.wq_check_workspace(ws)
+    print(json.dumps({"profile_config": p.name, "M": p.M, "N": p.N, "K": p.K, "calls": args.calls}))
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
+    if args.profile_config:
+        return main_profile(args)
     if args.impl == "reference":
         return main_reference(args)
     return main_ours(args)

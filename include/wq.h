@@ -33,7 +33,8 @@
  *
  * Arguments: bits in {2, 3, 4}; group in {32, 64, 128}; K % group == 0;
  * 0 <= M <= 16; N, K >= 0.  x and wq must be 16-byte aligned, y 4-byte
- * aligned, scales 2-byte aligned.  Streams are passed as `void*` holding a
+ * aligned, scales 2-byte aligned (16-byte aligned scales and zeros take a
+ * faster path in wq_gemm).  Streams are passed as `void*` holding a
  * cudaStream_t (NULL = the legacy default stream).  Every call is
  * asynchronous on its stream and returns a status; kernels never trap:
  * invalid arguments are rejected on the host before anything is launched.

@@ -289,6 +289,8 @@ wq_status_t wq_gemm(const uint16_t* x, const uint32_t* wq, const uint16_t* scale
     a.I = I;
     a.U = static_cast<long long>(T) * I;
     a.P = wq::choose_grid(T, I, d->sm_count);
+    const int gps = wq::stage_values(bits) / group;
+    a.meta_vec = (a.ng % gps == 0 && aligned(scales, 16) && aligned(zeros, 16)) ? 1 : 0;
 
     cudaError_t e;
     if (bits == 4)

@@ -30,6 +30,7 @@ struct GemmArgs {
     int T, I;         // tiles, k-stages per tile
     long long U;      // T * I work units
     int P;            // CTAs
+    int meta_vec;     // scales/zeros 16-byte aligned and K/group a multiple of the groups per stage
 };
 
 // Static stream-K schedule: CTA b owns units [unit_begin(b), unit_begin(b+1)).
