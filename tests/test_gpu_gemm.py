@@ -26,7 +26,7 @@ def _wq():
 
 FORMATS = [(4, 128), (4, 64), (4, 32), (2, 64), (2, 128), (2, 32), (3, 128), (3, 64), (3, 32)]
 SHAPES = [(1, 1, 128), (3, 130, 384), (16, 300, 1280), (8, 257, 2048), (9, 128, 640),
-          (12, 513, 4480)]
+          (12, 513, 4480), (5, 200, 1056)]
 
 
 def _fid(f):

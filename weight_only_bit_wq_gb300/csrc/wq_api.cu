@@ -7,7 +7,7 @@
 #include <mutex>
 #include <vector>
 
-#include "../../include/wq.h"
+#include "wq.h"
 #include "wq_internal.h"
 
 namespace {
@@ -187,6 +187,21 @@ wq_status_t wq_workspace_init(void* workspace, size_t bytes, void* stream) {
 
 namespace {
 
+// X as one 3-D box per stage: dims {64 values, M rows, K/64 chunks}, the
+// chunk stride 128 bytes, so a box of {64, 16, c} lands in shared memory as c
+// consecutive [16 rows][128 bytes] swizzled tiles.  Requires K % 64 == 0 (a
+// partial chunk would alias the next row instead of reading zeros).
+wq_status_t encode_x3d(const uint16_t* x, int M, int K, int chunks, CUtensorMap* tmX) {
+    const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(M), static_cast<cuuint64_t>(K / 64)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * 2, 128};
+    const cuuint32_t box[3] = {64, 16, static_cast<cuuint32_t>(chunks)};
+    const cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = g_encode(tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(x), dims,
+                          strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? WQ_OK : WQ_ERR_INVALID_ARG;
+}
+
 wq_status_t encode_maps(const uint16_t* x, const uint32_t* wq, int M, int N, int K, int W, int nt,
                         CUtensorMap* tmW, CUtensorMap* tmX) {
     if (wq_status_t st = get_encoder()) return st;
@@ -259,9 +274,11 @@ wq_status_t wq_gemm(const uint16_t* x, const uint32_t* wq, const uint16_t* scale
     if (wq_status_t st = device_info(&d)) return st;
 
     const int W = static_cast<int>(wq_packed_words_per_row(K, bits));
-    const int nt = M <= 8 ? 1 : 2;
+    const bool tc = (bits == 4 || bits == 2);  // tensor-core kernel: X tile always 16 rows
+    const int nt = (tc || M > 8) ? 2 : 1;
     const int T = (N + wq::kBN - 1) / wq::kBN;
-    const int I = (K + wq::stage_values(bits) - 1) / wq::stage_values(bits);
+    const int sv = (bits == 4 || bits == 2) ? wq::tc_stage_values(bits) : wq::stage_values(bits);
+    const int I = (K + sv - 1) / sv;
     const WsLayout lay = ws_layout(T, d->sm_count);
     void* ws = workspace;
     if (!ws) {
@@ -272,6 +289,9 @@ wq_status_t wq_gemm(const uint16_t* x, const uint32_t* wq, const uint16_t* scale
 
     CUtensorMap tmW, tmX;
     if (wq_status_t st = encode_maps(x, wq, M, N, K, W, nt, &tmW, &tmX)) return st;
+    const bool x3d = tc && K % 64 == 0;
+    if (x3d)
+        if (wq_status_t st = encode_x3d(x, M, K, sv / 64, &tmX)) return st;
 
     wq::GemmArgs a;
     a.scales = scales;
@@ -289,14 +309,15 @@ wq_status_t wq_gemm(const uint16_t* x, const uint32_t* wq, const uint16_t* scale
     a.I = I;
     a.U = static_cast<long long>(T) * I;
     a.P = wq::choose_grid(T, I, d->sm_count);
-    const int gps = wq::stage_values(bits) / group;
+    const int gps = sv / group;
     a.meta_vec = (a.ng % gps == 0 && aligned(scales, 16) && aligned(zeros, 16)) ? 1 : 0;
+    a.x3d = x3d ? 1 : 0;
 
     cudaError_t e;
     if (bits == 4)
-        e = wq::launch_gemm_b4(group, nt, tmW, tmX, a, s);
+        e = wq::launch_gemm_tc_b4(group, tmW, tmX, a, s);
     else if (bits == 2)
-        e = wq::launch_gemm_b2(group, nt, tmW, tmX, a, s);
+        e = wq::launch_gemm_tc_b2(group, tmW, tmX, a, s);
     else
         e = wq::launch_gemm_b3(group, nt, tmW, tmX, a, s);
     if (e == cudaErrorNotSupported) return WQ_ERR_UNSUPPORTED;

@@ -7,7 +7,7 @@
 #include <mutex>
 #include <vector>
 
-#include "../../include/wq.h"
+#include "wq.h"
 #include "wq_internal.h"
 
 namespace {

@@ -18,6 +18,9 @@ constexpr size_t kWsHeader = 256;                    // error word + padding
 // Values per packed word and per stage.
 constexpr int values_per_word(int bits) { return bits == 4 ? 8 : bits == 3 ? 10 : 16; }
 constexpr int stage_values(int bits) { return kWordsPerStage * values_per_word(bits); }
+// The tensor-core kernel reads tc_boxes(bits) adjacent 32-word boxes per row per stage.
+constexpr int tc_boxes(int bits) { return bits == 4 ? 2 : 1; }
+constexpr int tc_stage_values(int bits) { return tc_boxes(bits) * stage_values(bits); }
 
 struct GemmArgs {
     const uint16_t* scales;
@@ -31,6 +34,7 @@ struct GemmArgs {
     long long U;      // T * I work units
     int P;            // CTAs
     int meta_vec;     // scales/zeros 16-byte aligned and K/group a multiple of the groups per stage
+    int x3d;          // X map is 3-D [K/64][M][64]: one TMA box per stage (K % 64 == 0)
 };
 
 // Static stream-K schedule: CTA b owns units [unit_begin(b), unit_begin(b+1)).
@@ -46,6 +50,12 @@ cudaError_t launch_gemm_b2(int group, int nt, const CUtensorMap& tmW, const CUte
                            const GemmArgs& a, cudaStream_t s);
 cudaError_t launch_gemm_b3(int group, int nt, const CUtensorMap& tmW, const CUtensorMap& tmX,
                            const GemmArgs& a, cudaStream_t s);
+
+// Tensor-core (tcgen05) kernels, 4-bit and 2-bit codes.
+cudaError_t launch_gemm_tc_b4(int group, const CUtensorMap& tmW, const CUtensorMap& tmX,
+                              const GemmArgs& a, cudaStream_t s);
+cudaError_t launch_gemm_tc_b2(int group, const CUtensorMap& tmW, const CUtensorMap& tmX,
+                              const GemmArgs& a, cudaStream_t s);
 
 // Elementwise kernels.
 cudaError_t launch_pack(const uint8_t* q, uint32_t* wq, int N, int K, int bits, int W,

@@ -6,7 +6,7 @@
 
 #include <new>
 
-#include "../../include/wq.h"
+#include "wq.h"
 
 struct wq_step_graph {
     cudaGraph_t graph = nullptr;
