@@ -36,10 +36,6 @@
 namespace wq {
 namespace tc {
 
-constexpr int kWarps = kConsumerWarps + 2;  // consumers, TMA producer, MMA issuer
-constexpr int kThreadsTc = 32 * kWarps;
-constexpr int kProducerWarp = kConsumerWarps;
-constexpr int kMmaWarp = kConsumerWarps + 1;
 constexpr int kN = 16;          // MMA N: rows of X (M padded to 16)
 constexpr uint32_t kTmemCols = 512;
 constexpr int kSmemBudgetTc = 210 * 1024;
@@ -60,8 +56,17 @@ struct Lay {
     static constexpr int kStageBytes = round_up_tc(kWBytes + kXBytes, 1024);
     static constexpr int kGPS = kStageValues / G;               // groups per stage
     static constexpr int kSteps = G / 16;                       // K16 steps per group
-    static constexpr int kHalfSteps = kSteps / 2;               // per consumer half
     static constexpr int kACols = kSteps * 8;                   // TMEM columns of one A tile
+    // Consumer warps: kSplit per TMEM lane quarter, each taking kStepsW of a
+    // group's K steps and kColsW of the accumulator's 16 columns.
+    static constexpr int kCW = 8;
+    static constexpr int kSplit = kCW / 4;
+    static constexpr int kStepsW = kSteps / kSplit;
+    static constexpr int kColsW = kN / kSplit;
+    static constexpr int kWordsW = BITS == 4 ? 2 * kStepsW : kStepsW;  // packed words per warp per group
+    static constexpr int kProducerWarp = kCW;
+    static constexpr int kMmaWarp = kCW + 1;
+    static constexpr int kThreads = 32 * (kCW + 2);
     static constexpr int kStages = clamp_tc(kSmemBudgetTc / kStageBytes, 2, 8);
     static constexpr int kBarOffset = kStages * kStageBytes;
     static constexpr int kSmemBytes = kBarOffset + 512 + 1024;  // barriers/flags + align slack
@@ -70,10 +75,14 @@ struct Lay {
     // batch's accumulators.  2 kR slots: a slot is rewritten two batches after
     // its last use, by which time its accumulator has been read.
     static constexpr int kR = kGPS / 2;
-    static constexpr int kSlotCols = kACols + kN;
     static constexpr int kNB = 2 * kR;
+    // Zero point on the tensor core where tensor memory allows: per group an
+    // 8-column tile holding -(128 + z) in every column of the row, and one
+    // more MMA per K step; otherwise q - z is formed on the CUDA cores.
+    static constexpr bool kZtc = (kNB * (kACols + 8) + 15) / 16 * 16 + kNB * kN <= kTmemCols;
     static constexpr uint32_t kColA = 0;                        // kNB A tiles
-    static constexpr uint32_t kColD = (kNB * kACols + 15) / 16 * 16;  // kNB accumulators
+    static constexpr uint32_t kColZ = kNB * kACols;             // kNB zero-point tiles
+    static constexpr uint32_t kColD = (kColZ + (kZtc ? kNB * 8 : 0) + 15) / 16 * 16;  // accumulators
     static_assert(kColD + kNB * kN <= kTmemCols, "tensor memory budget");
     static_assert(kColD % 16 == 0, "accumulators 16-column aligned");
 };
@@ -156,6 +165,10 @@ struct RowMeta {
     __device__ __forceinline__ uint32_t zero_point(int gi) const {
         return __byte_perm(z[gi / 4], 0x43u, 0x4040u | (0x0101u * static_cast<uint32_t>(gi & 3)));
     }
+    // bf16x2 (-(128 + z), -(128 + z)): high byte 0xC3.
+    __device__ __forceinline__ uint32_t neg_zero_point(int gi) const {
+        return __byte_perm(z[gi / 4], 0xc3u, 0x4040u | (0x0101u * static_cast<uint32_t>(gi & 3)));
+    }
 };
 
 // bf16x2 (128 + lo, 128 + hi) from the low nibble (or 2-bit field, per
@@ -164,31 +177,40 @@ __device__ __forceinline__ uint32_t magic_bytes(uint32_t a, uint32_t b, uint32_t
     return lop3_and_or(__byte_perm(a, b, sel), mask, 0x43004300u);
 }
 
-// Eight bf16x2 registers of q - z (k = 0..15 in natural order) from two 4-bit
-// words; zz = bf16x2 (128 + z, 128 + z), so each subtraction is exact.
-__device__ __forceinline__ void unpack4_k16(uint32_t w0, uint32_t w1, uint32_t zz, uint32_t (&p)[8]) {
-    const uint32_t v0 = w0 >> 4, v1 = w1 >> 4;
-    p[0] = bf16x2_sub(magic_bytes(w0, v0, 0x4400u, 0x000f000fu), zz);
-    p[1] = bf16x2_sub(magic_bytes(w0, v0, 0x5511u, 0x000f000fu), zz);
-    p[2] = bf16x2_sub(magic_bytes(w0, v0, 0x6622u, 0x000f000fu), zz);
-    p[3] = bf16x2_sub(magic_bytes(w0, v0, 0x7733u, 0x000f000fu), zz);
-    p[4] = bf16x2_sub(magic_bytes(w1, v1, 0x4400u, 0x000f000fu), zz);
-    p[5] = bf16x2_sub(magic_bytes(w1, v1, 0x5511u, 0x000f000fu), zz);
-    p[6] = bf16x2_sub(magic_bytes(w1, v1, 0x6622u, 0x000f000fu), zz);
-    p[7] = bf16x2_sub(magic_bytes(w1, v1, 0x7733u, 0x000f000fu), zz);
+// Optional exact bf16x2 subtraction of zz = (128 + z, 128 + z).
+template <bool SUB>
+__device__ __forceinline__ uint32_t minus_zero(uint32_t v, uint32_t zz) {
+    return SUB ? bf16x2_sub(v, zz) : v;
 }
 
-// Eight bf16x2 registers of q - z (k = 0..15 in natural order) from one 2-bit word.
+// Eight bf16x2 registers (k = 0..15 in natural order) from two 4-bit words:
+// q - z if SUB, else 128 + q.
+template <bool SUB>
+__device__ __forceinline__ void unpack4_k16(uint32_t w0, uint32_t w1, uint32_t zz, uint32_t (&p)[8]) {
+    const uint32_t v0 = w0 >> 4, v1 = w1 >> 4;
+    p[0] = minus_zero<SUB>(magic_bytes(w0, v0, 0x4400u, 0x000f000fu), zz);
+    p[1] = minus_zero<SUB>(magic_bytes(w0, v0, 0x5511u, 0x000f000fu), zz);
+    p[2] = minus_zero<SUB>(magic_bytes(w0, v0, 0x6622u, 0x000f000fu), zz);
+    p[3] = minus_zero<SUB>(magic_bytes(w0, v0, 0x7733u, 0x000f000fu), zz);
+    p[4] = minus_zero<SUB>(magic_bytes(w1, v1, 0x4400u, 0x000f000fu), zz);
+    p[5] = minus_zero<SUB>(magic_bytes(w1, v1, 0x5511u, 0x000f000fu), zz);
+    p[6] = minus_zero<SUB>(magic_bytes(w1, v1, 0x6622u, 0x000f000fu), zz);
+    p[7] = minus_zero<SUB>(magic_bytes(w1, v1, 0x7733u, 0x000f000fu), zz);
+}
+
+// Eight bf16x2 registers (k = 0..15 in natural order) from one 2-bit word:
+// q - z if SUB, else 128 + q.
+template <bool SUB>
 __device__ __forceinline__ void unpack2_k16(uint32_t w, uint32_t zz, uint32_t (&p)[8]) {
     const uint32_t u1 = w >> 2, u2 = w >> 4, u3 = w >> 6;
-    p[0] = bf16x2_sub(magic_bytes(w, u1, 0x4400u, 0x00030003u), zz);
-    p[1] = bf16x2_sub(magic_bytes(u2, u3, 0x4400u, 0x00030003u), zz);
-    p[2] = bf16x2_sub(magic_bytes(w, u1, 0x5511u, 0x00030003u), zz);
-    p[3] = bf16x2_sub(magic_bytes(u2, u3, 0x5511u, 0x00030003u), zz);
-    p[4] = bf16x2_sub(magic_bytes(w, u1, 0x6622u, 0x00030003u), zz);
-    p[5] = bf16x2_sub(magic_bytes(u2, u3, 0x6622u, 0x00030003u), zz);
-    p[6] = bf16x2_sub(magic_bytes(w, u1, 0x7733u, 0x00030003u), zz);
-    p[7] = bf16x2_sub(magic_bytes(u2, u3, 0x7733u, 0x00030003u), zz);
+    p[0] = minus_zero<SUB>(magic_bytes(w, u1, 0x4400u, 0x00030003u), zz);
+    p[1] = minus_zero<SUB>(magic_bytes(u2, u3, 0x4400u, 0x00030003u), zz);
+    p[2] = minus_zero<SUB>(magic_bytes(w, u1, 0x5511u, 0x00030003u), zz);
+    p[3] = minus_zero<SUB>(magic_bytes(u2, u3, 0x5511u, 0x00030003u), zz);
+    p[4] = minus_zero<SUB>(magic_bytes(w, u1, 0x6622u, 0x00030003u), zz);
+    p[5] = minus_zero<SUB>(magic_bytes(u2, u3, 0x6622u, 0x00030003u), zz);
+    p[6] = minus_zero<SUB>(magic_bytes(w, u1, 0x7733u, 0x00030003u), zz);
+    p[7] = minus_zero<SUB>(magic_bytes(u2, u3, 0x7733u, 0x00030003u), zz);
 }
 
 __device__ __forceinline__ void record_error_tc(const GemmArgs& a, volatile int* abort_flag) {
@@ -215,9 +237,11 @@ __device__ __forceinline__ void load_words(const uint8_t* row, int wi0, int r, u
     }
 }
 
-// Segment end for one thread (row r, columns 8h .. 8h + 7): store Y, or publish
-// the partial and let the last CTA of the tile sum all partials in k order.
-__device__ __forceinline__ void finish_tile(const GemmArgs& a, const float (&acc)[8], int t,
+// Segment end for one thread (row r, columns C h .. C h + C - 1): store Y, or
+// publish the partial and let the last CTA of the tile sum all partials in k
+// order.  NCT = consumer threads (named barrier 1).
+template <int C, int NCT>
+__device__ __forceinline__ void finish_tile(const GemmArgs& a, const float (&acc)[C], int t,
                                            bool whole, long long u_lo, int r, int h, int tid,
                                            bool dead, volatile int* abort_flag,
                                            volatile int* last_flag) {
@@ -225,16 +249,16 @@ __device__ __forceinline__ void finish_tile(const GemmArgs& a, const float (&acc
     if (whole) {
         if (!dead && n < a.N)
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-                if (8 * h + j < a.M) a.y[static_cast<size_t>(8 * h + j) * a.N + n] = acc[j];
+            for (int j = 0; j < C; ++j)
+                if (C * h + j < a.M) a.y[static_cast<size_t>(C * h + j) * a.N + n] = acc[j];
         return;
     }
     const int t_first = static_cast<int>(u_lo / a.I);
     float* mine = a.partials + static_cast<size_t>(2 * blockIdx.x + (t == t_first ? 0 : 1)) *
                                    (kMaxCols * kBN);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) __stcg(mine + (8 * h + j) * kBN + r, acc[j]);
-    named_bar_sync(1, 32 * kConsumerWarps);
+    for (int j = 0; j < C; ++j) __stcg(mine + (C * h + j) * kBN + r, acc[j]);
+    named_bar_sync(1, NCT);
     const long long tu0 = static_cast<long long>(t) * a.I;
     const int b_first = static_cast<int>(((tu0 + 1) * a.P + a.U - 1) / a.U - 1);
     const int b_last = static_cast<int>(((tu0 + a.I) * a.P + a.U - 1) / a.U - 1);
@@ -246,34 +270,34 @@ __device__ __forceinline__ void finish_tile(const GemmArgs& a, const float (&acc
             *last_flag = (prev == b_last - b_first) ? 1 : 0;
         }
     }
-    named_bar_sync(1, 32 * kConsumerWarps);
+    named_bar_sync(1, NCT);
     if (*last_flag) {
-        float tot[8];
+        float tot[C];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) tot[j] = 0.f;
+        for (int j = 0; j < C; ++j) tot[j] = 0.f;
         for (int b = b_first; b <= b_last; ++b) {
             if (b == static_cast<int>(blockIdx.x)) {
 #pragma unroll
-                for (int j = 0; j < 8; ++j) tot[j] += acc[j];
+                for (int j = 0; j < C; ++j) tot[j] += acc[j];
             } else {
                 const int tb = static_cast<int>((a.U * b / a.P) / a.I);
                 const float* src = a.partials +
                                    static_cast<size_t>(2 * b + (t == tb ? 0 : 1)) * (kMaxCols * kBN);
 #pragma unroll
-                for (int j = 0; j < 8; ++j) tot[j] += __ldcg(src + (8 * h + j) * kBN + r);
+                for (int j = 0; j < C; ++j) tot[j] += __ldcg(src + (C * h + j) * kBN + r);
             }
         }
         if (n < a.N)
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-                if (8 * h + j < a.M) a.y[static_cast<size_t>(8 * h + j) * a.N + n] = tot[j];
+            for (int j = 0; j < C; ++j)
+                if (C * h + j < a.M) a.y[static_cast<size_t>(C * h + j) * a.N + n] = tot[j];
         if (tid == 0) a.counters[t] = 0;
     }
-    named_bar_sync(1, 32 * kConsumerWarps);
+    named_bar_sync(1, NCT);
 }
 
 template <int BITS, int G>
-__global__ void __launch_bounds__(kThreadsTc, 1)
+__global__ void __launch_bounds__(Lay<BITS, G>::kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                    const GemmArgs a) {
     using L = Lay<BITS, G>;
@@ -294,10 +318,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < S; ++i) {
             mbar_init(&full[i], 1);
-            mbar_init(&empty[i], kConsumerWarps + 1);  // consumers read W, MMAs read X
+            mbar_init(&empty[i], L::kCW + 1);  // consumers read W, MMAs read X
         }
         for (int i = 0; i < L::kNB; ++i) {
-            mbar_init(&filled[i], kConsumerWarps);
+            mbar_init(&filled[i], L::kCW);
             mbar_init(&done[i], 1);
         }
         mbar_init(drain, 1);
@@ -305,7 +329,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         *last_flag = 0;
         fence_mbar_init();
     }
-    if (warp == kMmaWarp) {
+    if (warp == L::kMmaWarp) {
         tmem_alloc(smem_addr(tmem_slot), kTmemCols);
         tmem_relinquish();
         tc_fence_before();
@@ -320,7 +344,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     const int t_first = static_cast<int>(u_lo / a.I);
     const int i_first = static_cast<int>(u_lo - static_cast<long long>(t_first) * a.I);
 
-    if (warp == kProducerWarp) {
+    if (warp == L::kProducerWarp) {
         // ------------------------------------------------------------ producer
         if (lane != 0) return;
         prefetch_tensormap(&tmW);
@@ -379,7 +403,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         return;
     }
 
-    if (warp == kMmaWarp) {
+    if (warp == L::kMmaWarp) {
         // --------------------------------------------------------- MMA issuer
         // The whole warp walks the schedule (uniform control flow); one
         // elected lane issues the MMAs and commits.
@@ -410,6 +434,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                         const uint64_t bdesc =
                             desc0 + static_cast<uint64_t>(((v0 / 64) * L::kXBoxBytes + (v0 % 64) * 2) >> 4);
                         tc_mma_ts(tD, tA + 8 * s, bdesc, kIdesc, s > 0 ? 1u : 0u);
+                        if (L::kZtc) tc_mma_ts(tD, tmem + L::kColZ + sb * 8, bdesc, kIdesc, 1u);
                     }
                     tc_commit(&done[sb]);
                     if (gi == L::kGPS - 1) tc_commit(&empty[slot]);
@@ -423,7 +448,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         __syncwarp();
         volatile int never = 0;
         mbar_wait(drain, 0, &never);
-        named_bar_sync(3, 32 * (kConsumerWarps + 1));
+        named_bar_sync(3, 32 * (L::kCW + 1));
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
         return;
@@ -432,17 +457,17 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     // ---------------------------------------------------------------- consumers
     const int tid = threadIdx.x;  // 0 .. 255
     const int q = warp & 3;       // TMEM lane quarter
-    const int h = warp >> 2;      // which half of each group's K steps (and of D's columns)
+    const int h = warp >> 2;      // which K steps of each group (and columns of D) this warp takes
     const int r = 32 * q + lane;  // tile row == TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(32 * q) << 16;
     const bool vec = a.meta_vec != 0;
-    constexpr int kWordsHalf = BITS == 4 ? G / 16 : G / 32;  // packed words per half group
     // After a failed wait a warp stops touching tensor memory but keeps
     // arriving on barriers and walking the named barriers of its siblings.
     bool dead = false;
-    float acc[8];
+    constexpr int C = L::kColsW;
+    float acc[C];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+    for (int j = 0; j < C; ++j) acc[j] = 0.f;
 
     using RM = RowMeta<L::kGPS>;
     int t = t_first, i = i_first;    // unit being computed
@@ -468,9 +493,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         return __uint_as_float((gi & 1) ? (w & 0xffff0000u) : (w << 16));
     };
     auto finish = [&](int tt, bool wh) {
-        finish_tile(a, acc, tt, wh, u_lo, r, h, tid, dead, abort_flag, last_flag);
+        finish_tile<C, 32 * L::kCW>(a, acc, tt, wh, u_lo, r, h, tid, dead, abort_flag, last_flag);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+        for (int j = 0; j < C; ++j) acc[j] = 0.f;
     };
     // Read back the accumulators of the kR groups [g0, g0 + kR), whose scales
     // are s[first .. first + kR), and add scale * D to acc.
@@ -482,16 +507,16 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         }
         if (dead) return;
         tc_fence_after();
-        uint32_t v[L::kR][8];
+        uint32_t v[L::kR][C];
 #pragma unroll
         for (int j = 0; j < L::kR; ++j)
-            tmem_ld8(tmem + L::kColD + ((g0 + j) % L::kNB) * kN + 8 * h + lane_off, v[j]);
+            tmem_ld_cols<C>(tmem + L::kColD + ((g0 + j) % L::kNB) * kN + C * h + lane_off, v[j]);
         tmem_wait_ld();
 #pragma unroll
         for (int j = 0; j < L::kR; ++j) {
             const float sc = scale_of(s, first + j);
 #pragma unroll
-            for (int jj = 0; jj < 8; ++jj) acc[jj] = fmaf(sc, __uint_as_float(v[j][jj]), acc[jj]);
+            for (int jj = 0; jj < C; ++jj) acc[jj] = fmaf(sc, __uint_as_float(v[j][jj]), acc[jj]);
         }
     };
     // Unpack and store the A tiles of groups [gb, gb + kR) of the stage.
@@ -501,22 +526,24 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             for (int j = 0; j < L::kR; ++j) {
                 const int gi = gb + j;
                 const uint32_t sb = (gl + j) % L::kNB;
-                uint32_t w[kWordsHalf];
+                uint32_t w[L::kWordsW];
                 const uint32_t zz = m.zero_point(gi);
-                const int wi = BITS == 4 ? gi * (G / 8) + h * (G / 16) : gi * (G / 16) + h * (G / 32);
-                load_words<kWordsHalf>(row0 + (wi / kWordsPerStage) * L::kBoxBytes,
+                const int wi = (BITS == 4 ? gi * (G / 8) : gi * (G / 16)) + h * L::kWordsW;
+                load_words<L::kWordsW>(row0 + (wi / kWordsPerStage) * L::kBoxBytes,
                                        wi % kWordsPerStage, r, w);
                 const uint32_t tA = tmem + L::kColA + sb * L::kACols + lane_off;
 #pragma unroll
-                for (int hs = 0; hs < L::kHalfSteps; ++hs) {
+                for (int hs = 0; hs < L::kStepsW; ++hs) {
                     uint32_t p[8];
                     if (BITS == 4) {
-                        unpack4_k16(w[2 * hs], w[2 * hs + 1], zz, p);
+                        unpack4_k16<!L::kZtc>(w[2 * hs], w[2 * hs + 1], zz, p);
                     } else {
-                        unpack2_k16(w[hs], zz, p);
+                        unpack2_k16<!L::kZtc>(w[hs], zz, p);
                     }
-                    tmem_st8(tA + 8 * (h * L::kHalfSteps + hs), p);
+                    tmem_st8(tA + 8 * (h * L::kStepsW + hs), p);
                 }
+                if (L::kZtc && h == 0)
+                    tmem_st8_same(tmem + L::kColZ + sb * 8 + lane_off, m.neg_zero_point(gi));
             }
             tmem_wait_st();
             tc_fence_before();
@@ -572,7 +599,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         read_batch(gl - L::kR, sprev, L::kR);
         finish(prev_t, prev_whole);
     }
-    named_bar_sync(3, 32 * (kConsumerWarps + 1));
+    named_bar_sync(3, 32 * (L::kCW + 1));
 }
 
 template <int BITS, int G>
@@ -583,7 +610,7 @@ cudaError_t launch_tc(const CUtensorMap& tmW, const CUtensorMap& tmX, const Gemm
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
     if (e != cudaSuccess) return e;
-    kern<<<a.P, kThreadsTc, L::kSmemBytes, s>>>(tmW, tmX, a);
+    kern<<<a.P, L::kThreads, L::kSmemBytes, s>>>(tmW, tmX, a);
     return cudaGetLastError();
 }
 
