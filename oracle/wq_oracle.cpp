@@ -21,11 +21,17 @@
 // * The pages never write the dequantisation formula, the bit order inside a
 //   word or the zero-point storage.  Readings taken here:
 //     - asymmetric affine dequantisation w = (q - z) * s, unsigned q, integer z;
-//     - codes are packed along K, LSB first: code k of a row sits in word
-//       k / vpw at bits [b*(k % vpw), b*(k % vpw) + b), vpw = 8 (b=4),
-//       10 (b=3, bits 30..31 zero), 16 (b=2); words run along K ignoring
-//       group boundaries; unused slots are zero; each row is padded with zero
-//       words to a multiple of 4 words (16 bytes);
+//     - codes are packed along K, vpw consecutive codes per 32-bit word,
+//       vpw = 8 (b=4), 10 (b=3), 16 (b=2); words run along K ignoring group
+//       boundaries.  Inside a word the even-numbered codes fill the low
+//       half-word and the odd-numbered codes the high half-word, each half
+//       least significant first: code k sits in word k / vpw, slot
+//       j = k % vpw, at bits [16*(j % 2) + b*(j / 2), ... + b).  (Load-time
+//       repacking is the pages' own step, so the word layout is the
+//       implementation's to choose; this one puts two neighbouring codes at
+//       the same place in the two 16-bit halves.)  For b = 3 bits 15 and 31
+//       stay zero; unused slots are zero; each row is padded with zero words
+//       to a multiple of 4 words (16 bytes);
 //     - only the low b bits of each code are stored;
 //     - scales are bf16 [N][K/G], zero points uint8 [N][K/G], both row-major;
 //     - X is bf16 [M][K] row-major, Y is [M][N] row-major.
@@ -50,6 +56,9 @@ int values_per_word(int bits) {
     if (bits == 2) return 16;
     return 0;
 }
+
+// First bit of slot j (0 <= j < vpw) inside its word.
+int slot_shift(int bits, int j) { return 16 * (j % 2) + bits * (j / 2); }
 
 double bf16_bits_to_double(uint16_t b) {
     uint32_t u = static_cast<uint32_t>(b) << 16;
@@ -82,7 +91,7 @@ int wqo_pack(const uint8_t* q, uint32_t* wq, int N, int K, int bits) {
             uint32_t code = static_cast<uint32_t>(q[n * K + k]) & mask;
             long word = k / vpw;
             int slot = static_cast<int>(k % vpw);
-            wq[n * W + word] |= code << (bits * slot);
+            wq[n * W + word] |= code << slot_shift(bits, slot);
         }
     }
     return 0;
@@ -97,7 +106,7 @@ int wqo_unpack(const uint32_t* wq, uint8_t* q, int N, int K, int bits) {
     for (long n = 0; n < N; ++n)
         for (long k = 0; k < K; ++k) {
             uint32_t word = wq[n * W + k / vpw];
-            q[n * K + k] = static_cast<uint8_t>((word >> (bits * (k % vpw))) & mask);
+            q[n * K + k] = static_cast<uint8_t>((word >> slot_shift(bits, static_cast<int>(k % vpw))) & mask);
         }
     return 0;
 }
@@ -112,7 +121,7 @@ int wqo_dequant_f64(const uint32_t* wq, const uint16_t* s, const uint8_t* z, dou
     uint32_t mask = (1u << bits) - 1u;
     for (long n = 0; n < N; ++n)
         for (long k = 0; k < K; ++k) {
-            uint32_t code = (wq[n * W + k / vpw] >> (bits * (k % vpw))) & mask;
+            uint32_t code = (wq[n * W + k / vpw] >> slot_shift(bits, static_cast<int>(k % vpw))) & mask;
             long g = k / G;
             double diff = static_cast<double>(code) - static_cast<double>(z[n * ng + g]);
             w[n * K + k] = diff * bf16_bits_to_double(s[n * ng + g]);

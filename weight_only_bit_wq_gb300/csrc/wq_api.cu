@@ -79,7 +79,8 @@ WsLayout ws_layout(int T, int sm_count) {
     const size_t partial_bytes =
         static_cast<size_t>(2) * sm_count * wq::kMaxCols * wq::kBN * sizeof(float);
     l.counter_off = l.partial_off + partial_bytes;
-    l.bytes = (l.counter_off + static_cast<size_t>(T) * sizeof(int) + 255) / 256 * 256;
+    l.bytes = (l.counter_off + static_cast<size_t>(T) * wq::kCountersPerTile * sizeof(int) + 255) /
+              256 * 256;
     return l;
 }
 
@@ -202,7 +203,7 @@ wq_status_t encode_x3d(const uint16_t* x, int M, int K, int chunks, CUtensorMap*
     return r == CUDA_SUCCESS ? WQ_OK : WQ_ERR_INVALID_ARG;
 }
 
-wq_status_t encode_maps(const uint16_t* x, const uint32_t* wq, int M, int N, int K, int W, int nt,
+wq_status_t encode_maps(const uint16_t* x, const uint32_t* wq, int M, int N, int K, int W,
                         CUtensorMap* tmW, CUtensorMap* tmX) {
     if (wq_status_t st = get_encoder()) return st;
     {
@@ -220,7 +221,7 @@ wq_status_t encode_maps(const uint16_t* x, const uint32_t* wq, int M, int N, int
     {
         const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
         const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
-        const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(8 * nt)};
+        const cuuint32_t box[2] = {64, 16};
         const cuuint32_t es[2] = {1, 1};
         CUresult r = g_encode(tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(x), dims,
                               strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -274,10 +275,8 @@ wq_status_t wq_gemm(const uint16_t* x, const uint32_t* wq, const uint16_t* scale
     if (wq_status_t st = device_info(&d)) return st;
 
     const int W = static_cast<int>(wq_packed_words_per_row(K, bits));
-    const bool tc = (bits == 4 || bits == 2);  // tensor-core kernel: X tile always 16 rows
-    const int nt = (tc || M > 8) ? 2 : 1;
     const int T = (N + wq::kBN - 1) / wq::kBN;
-    const int sv = (bits == 4 || bits == 2) ? wq::tc_stage_values(bits) : wq::stage_values(bits);
+    const int sv = wq::tc_stage_values(bits, group);
     const int I = (K + sv - 1) / sv;
     const WsLayout lay = ws_layout(T, d->sm_count);
     void* ws = workspace;
@@ -288,8 +287,8 @@ wq_status_t wq_gemm(const uint16_t* x, const uint32_t* wq, const uint16_t* scale
     }
 
     CUtensorMap tmW, tmX;
-    if (wq_status_t st = encode_maps(x, wq, M, N, K, W, nt, &tmW, &tmX)) return st;
-    const bool x3d = tc && K % 64 == 0;
+    if (wq_status_t st = encode_maps(x, wq, M, N, K, W, &tmW, &tmX)) return st;
+    const bool x3d = K % 64 == 0;
     if (x3d)
         if (wq_status_t st = encode_x3d(x, M, K, sv / 64, &tmX)) return st;
 
@@ -310,16 +309,17 @@ wq_status_t wq_gemm(const uint16_t* x, const uint32_t* wq, const uint16_t* scale
     a.U = static_cast<long long>(T) * I;
     a.P = wq::choose_grid(T, I, d->sm_count);
     const int gps = sv / group;
-    a.meta_vec = (a.ng % gps == 0 && aligned(scales, 16) && aligned(zeros, 16)) ? 1 : 0;
+    const bool gps_pow2 = (gps & (gps - 1)) == 0;
+    a.meta_vec = (gps_pow2 && a.ng % gps == 0 && aligned(scales, 16) && aligned(zeros, 16)) ? 1 : 0;
     a.x3d = x3d ? 1 : 0;
 
     cudaError_t e;
     if (bits == 4)
         e = wq::launch_gemm_tc_b4(group, tmW, tmX, a, s);
-    else if (bits == 2)
-        e = wq::launch_gemm_tc_b2(group, tmW, tmX, a, s);
+    else if (bits == 3)
+        e = wq::launch_gemm_tc_b3(group, tmW, tmX, a, s);
     else
-        e = wq::launch_gemm_b3(group, nt, tmW, tmX, a, s);
+        e = wq::launch_gemm_tc_b2(group, tmW, tmX, a, s);
     if (e == cudaErrorNotSupported) return WQ_ERR_UNSUPPORTED;
     return e == cudaSuccess ? WQ_OK : cuda_fail(e);
 }

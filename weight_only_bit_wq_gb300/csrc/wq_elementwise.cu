@@ -1,9 +1,11 @@
 // Load-time repacking and streaming dequantisation (one thread per packed word).
 //
-// Layout: code k of a row sits in word k / vpw at bits [b*(k % vpw), +b),
-// least significant first (vpw = 8, 10, 16 for b = 4, 3, 2); rows hold W words,
-// W a multiple of 4; unused slots and padding words are zero.  Repacking at
-// load time: Agens Engine page, section "功能" (加载时重新打包).
+// Layout: code k of a row sits in word k / vpw (vpw = 8, 10, 16 for b = 4, 3,
+// 2), slot j = k % vpw, at bits [16 (j % 2) + b (j / 2), +b): even slots fill
+// the low half-word and odd slots the high half-word, each half least
+// significant first.  Rows hold W words, W a multiple of 4; unused slots, pad
+// bits and padding words are zero.  Repacking at load time: Agens Engine page,
+// section "功能" (加载时重新打包).
 #include <cuda_bf16.h>
 #include "wq_internal.h"
 
@@ -11,6 +13,9 @@ namespace wq {
 namespace {
 
 __device__ __forceinline__ int vpw_of(int bits) { return bits == 4 ? 8 : bits == 3 ? 10 : 16; }
+
+// First bit of slot j inside its word.
+__device__ __forceinline__ int slot_shift(int bits, int j) { return 16 * (j & 1) + bits * (j >> 1); }
 
 __global__ void pack_kernel(const uint8_t* __restrict__ q, uint32_t* __restrict__ wq, int N, int K,
                             int bits, int W) {
@@ -26,7 +31,7 @@ __global__ void pack_kernel(const uint8_t* __restrict__ q, uint32_t* __restrict_
         uint32_t word = 0;
         for (int j = 0; j < vpw; ++j) {
             const int k = k0 + j;
-            if (k < K) word |= (static_cast<uint32_t>(row[k]) & mask) << (bits * j);
+            if (k < K) word |= (static_cast<uint32_t>(row[k]) & mask) << slot_shift(bits, j);
         }
         wq[idx] = word;
     }
@@ -47,7 +52,7 @@ __global__ void unpack_kernel(const uint32_t* __restrict__ wq, uint8_t* __restri
         uint8_t* row = q + n * K;
         for (int j = 0; j < vpw; ++j) {
             const int k = k0 + j;
-            if (k < K) row[k] = static_cast<uint8_t>((word >> (bits * j)) & mask);
+            if (k < K) row[k] = static_cast<uint8_t>((word >> slot_shift(bits, j)) & mask);
         }
     }
 }
@@ -73,7 +78,7 @@ __global__ void dequant_kernel(const uint32_t* __restrict__ wq, const uint16_t* 
             const int k = k0 + j;
             if (k >= K) break;
             const int gidx = k / group;
-            const int code = static_cast<int>((word >> (bits * j)) & mask);
+            const int code = static_cast<int>((word >> slot_shift(bits, j)) & mask);
             const int zp = zeros[n * ng + gidx];
             const float s = __uint_as_float(static_cast<uint32_t>(scales[n * ng + gidx]) << 16);
             const float v = static_cast<float>(code - zp) * s;

@@ -13,7 +13,7 @@
 namespace {
 
 // Fixed scratch size.  Enough for the split-K partials of up to 2 x (SM count)
-// CTAs (2.5 MB on a 152-SM GB300) plus one counter per 128-row tile.
+// CTAs (2.5 MB on a 152-SM GB300) plus eight counters per 128-row tile.
 constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
@@ -62,13 +62,13 @@ extern "C" wq_status_t wq_gemm_noalloc(const uint16_t* x, const uint32_t* wq,
     const long long tiles = (static_cast<long long>(N) + wq::kBN - 1) / wq::kBN;
     const size_t counter_off =
         wq::kWsHeader + size_t(2) * d->sm_count * wq::kMaxCols * wq::kBN * sizeof(float);
-    const size_t need = counter_off + static_cast<size_t>(tiles) * sizeof(int);
+    const size_t counter_bytes = static_cast<size_t>(tiles) * wq::kCountersPerTile * sizeof(int);
+    const size_t need = counter_off + counter_bytes;
     if (need > kNoAllocScratchBytes) return WQ_ERR_INVALID_ARG;
     // The array keeps whatever the previous call left: re-zero the arrival
     // counters, which must start at zero.
     if (tiles > 0 &&
-        cudaMemsetAsync(d->scratch + counter_off, 0, static_cast<size_t>(tiles) * sizeof(int), s) !=
-            cudaSuccess)
+        cudaMemsetAsync(d->scratch + counter_off, 0, counter_bytes, s) != cudaSuccess)
         return WQ_ERR_CUDA;
     return wq_gemm(x, wq, scales, zeros, y, M, N, K, group, bits, d->scratch,
                    kNoAllocScratchBytes, stream);

@@ -1,53 +1,87 @@
 // Weight-only low-bit skinny GEMM on the 5th-generation tensor core (sm_103a):
-//     Y[M][N] = X[M][K] . dequant(Wq)[N][K]^T,  M <= 16.
+//     Y[M][N] = X[M][K] . dequant(Wq)[N][K]^T,  M <= 16, 2/3/4-bit codes.
 //
 // A decode-step projection streams every packed weight once and multiplies it,
 // while on chip, against all stacked rows of X on tensor cores (OpenJet news
 // page, paragraph "并行解码的原理").  One CTA per SM, persistent, stream-K over
-// (128-row tile, k-stage) units exactly as the split depends on (N, K, bits,
-// group, SM count) only.  Ten warps:
+// (128-row tile, k-stage) units; the split depends on (N, K, bits, group, SM
+// count) only.  Warp roles (warp-specialised, connected by mbarrier rings):
 //
-// * warp 8  — TMA producer: per stage one 128-row x 128-byte tile of packed
-//   words and the matching X slice (16 rows x stage width, rows >= M read as
-//   zero), both 128-byte swizzled, into a ring of shared-memory stages;
-// * warp 9  — allocates tensor memory and, from one lane, issues the MMAs:
+// * TMA producer (one lane): per stage one or two 128-row x 128-byte boxes of
+//   packed words and the matching X slice (16 rows x stage width, rows >= M
+//   read as zero), all 128-byte swizzled, into a ring of shared-memory stages;
+// * unpack warps (two per TMEM lane quarter, each taking half of every
+//   group's K steps): one weight row per thread.  The "magic number" trick
+//   turns codes into bf16 — a code q placed in the mantissa of 128.0 reads as
+//   128 + q exactly — and the word layout (even-numbered codes in the low
+//   half-word, odd-numbered in the high half-word) makes one shift and one
+//   LOP3 produce the bf16 pair of two neighbouring codes.  The pairs go to
+//   tensor memory (tcgen05.st) as the MMA's A tile;
+// * MMA issuer (one elected lane; the warp also owns the TMEM allocation):
 //   tcgen05.mma kind::f16, M = 128 weight rows, N = 16 rows of X, K = 16,
-//   A (the weights) from tensor memory, B (X) straight from the swizzled
-//   shared tile through a matrix descriptor, fp32 D in tensor memory;
-// * warps 0..7 — one weight row per thread (warp w owns TMEM lanes
-//   32 (w % 4) .. +31; warps w and w + 4 split each group's K steps).  Each
-//   thread unpacks its row's codes with the bf16 "magic number" trick (code q
-//   lands in the mantissa of 128.0, giving 128 + q exactly) and stores them to
-//   tensor memory as the A tile in natural k order.  The zero point is applied
-//   on the tensor core too: a second MMA per K step multiplies the same X by
-//   a constant A tile holding -(128 + z) in every column of the row, so each
-//   group's D is sum_k x (q - z) up to fp32 accumulation.  The thread then
-//   reads its row of the group's D back with tcgen05.ld and adds scale * D to
-//   its fp32 accumulators.
+//   A from tensor memory, B (X) straight from the swizzled shared tile
+//   through a matrix descriptor, fp32 D per group in tensor memory.  The zero
+//   point is applied on the tensor core: a second MMA per K step multiplies
+//   the same X by a constant A tile holding -(128 + z) in every column of the
+//   row, so each group's D is sum_k x (q - z) (where tensor memory is too
+//   small for those tiles, q - z is formed on the CUDA cores instead);
+// * epilogue warps (one per lane quarter): write the zero-point tiles, read
+//   each group's D back (tcgen05.ld), add scale * D to the row's 16 fp32
+//   sums, and store Y or publish a split-K partial.
 //
+// Tensor memory holds rings of A-tile batch slots and accumulator slots, so
+// the unpack warps run ahead of the tensor core and never wait for a result.
 // Per group the D accumulation order is fixed (data MMA then zero-point MMA
 // per K step, K steps ascending) and the columns of one MMA never interact,
 // so a row of X gives bit-identical results alone or stacked.  A tile split
 // across CTAs is summed by the last CTA to finish it, in k order.
 #pragma once
+#include <type_traits>
+
 #include "wq_internal.h"
 #include "wq_ptx.cuh"
 
 namespace wq {
 namespace tc {
 
-constexpr int kN = 16;          // MMA N: rows of X (M padded to 16)
+constexpr int kN = 16;  // MMA N: rows of X (M padded to 16)
 constexpr uint32_t kTmemCols = 512;
 constexpr int kSmemBudgetTc = 210 * 1024;
+// Unpack warps per TMEM lane quarter (each takes 1 / kSplitWarps of a
+// group's K steps): two per lane quarter measured best; more add per-warp
+// overhead without adding ALU throughput.
+constexpr int kSplitWarps = 2;
+// TMEM columns per tcgen05.st of the unpacked A tile: one K step (8 columns)
+// per store lets the stores start while the rest of the group is unpacked.
+constexpr int kStoreCols = 8;
+constexpr uint32_t kFull = 0xffffffffu;
 
 constexpr int round_up_tc(int v, int a) { return (v + a - 1) / a * a; }
 constexpr int clamp_tc(int v, int lo, int hi) { return v < lo ? lo : (v > hi ? hi : v); }
 
+// Tensor-memory plan for batch slots of R groups: returns 100 z + 10 na + nd
+// for the first of (zero point on the tensor core z, na A slots, nd
+// accumulator slots) that fits, trying z = 1 before z = 0, then two
+// accumulator slots before one, then three A slots before two; 0 if none fits.
+constexpr int tmem_plan(int R, int a_cols, int n, int cols) {
+    for (int z = 1; z >= 0; --z)
+        for (int nd = 2; nd >= 1; --nd)
+            for (int na = 3; na >= 2; --na)
+                if (round_up_tc(na * R * (a_cols + 8 * z), 16) + nd * R * n <= cols)
+                    return 100 * z + 10 * na + nd;
+    return 0;
+}
+
 template <int BITS, int G>
 struct Lay {
-    static constexpr int kBoxes = tc_boxes(BITS);               // 32-word boxes per row
-    static constexpr int kStageValues = tc_stage_values(BITS);  // 512 (4-bit), 512 (2-bit)
-    static constexpr int kBoxBytes = kBN * kWordsPerStage * 4;  // 16 KB: 128 rows x 128 bytes
+    static constexpr int kVpw = values_per_word(BITS);
+    static constexpr int kPpw = kVpw / 2;                    // bf16 pairs per word
+    static constexpr int kBoxes = tc_boxes(BITS, G);         // 32-word boxes per row per stage
+    static constexpr int kStageWords = kBoxes * kWordsPerStage;
+    static constexpr int kStageValues = kStageWords * kVpw;
+    static_assert(kStageValues % G == 0, "whole groups per stage");
+    static_assert(kStageValues % 64 == 0, "whole 64-value X boxes per stage");
+    static constexpr int kBoxBytes = kBN * kWordsPerStage * 4;  // 16 KB
     static constexpr int kWBytes = kBoxes * kBoxBytes;
     static constexpr int kXBoxValues = 64;                      // 128 bytes of bf16
     static constexpr int kXBoxes = kStageValues / kXBoxValues;
@@ -57,34 +91,38 @@ struct Lay {
     static constexpr int kGPS = kStageValues / G;               // groups per stage
     static constexpr int kSteps = G / 16;                       // K16 steps per group
     static constexpr int kACols = kSteps * 8;                   // TMEM columns of one A tile
-    // Consumer warps: kSplit per TMEM lane quarter, each taking kStepsW of a
-    // group's K steps and kColsW of the accumulator's 16 columns.
-    static constexpr int kCW = 8;
-    static constexpr int kSplit = kCW / 4;
-    static constexpr int kStepsW = kSteps / kSplit;
-    static constexpr int kColsW = kN / kSplit;
-    static constexpr int kWordsW = BITS == 4 ? 2 * kStepsW : kStepsW;  // packed words per warp per group
-    static constexpr int kProducerWarp = kCW;
-    static constexpr int kMmaWarp = kCW + 1;
-    static constexpr int kThreads = 32 * (kCW + 2);
+    // Warp roles: kUW unpack warps (kSplit per TMEM lane quarter, each taking
+    // kStepsW of every group's K steps), four epilogue warps (one per lane
+    // quarter, all 16 accumulator columns), one TMA producer, one MMA issuer.
+    static constexpr int kSplit = (kSteps >= kSplitWarps) ? kSplitWarps : kSteps;
+    static constexpr int kUW = 4 * kSplit;
+    static constexpr int kEW = 4;
+    static constexpr int kProducerWarp = kUW + kEW;
+    static constexpr int kMmaWarp = kProducerWarp + 1;
+    static constexpr int kThreads = 32 * (kMmaWarp + 1);
+    static constexpr int kStepsW = kSteps / kSplit;             // K steps per warp per group
+    static constexpr int kPairsW = 8 * kStepsW;                 // bf16 pairs per thread per group
+    // A stage's groups go through the tensor core in two batches, [0, kR0)
+    // and [kR0, kGPS); a batch slot in tensor memory holds kR0 groups.
+    static constexpr int kR0 = (kGPS + 1) / 2;
     static constexpr int kStages = clamp_tc(kSmemBudgetTc / kStageBytes, 2, 8);
     static constexpr int kBarOffset = kStages * kStageBytes;
     static constexpr int kSmemBytes = kBarOffset + 512 + 1024;  // barriers/flags + align slack
-    // Consumers work in batches of kR groups (half a stage): unpack and store a
-    // batch's A tiles, retire the stores once, then read back the previous
-    // batch's accumulators.  2 kR slots: a slot is rewritten two batches after
-    // its last use, by which time its accumulator has been read.
-    static constexpr int kR = kGPS / 2;
-    static constexpr int kNB = 2 * kR;
-    // Zero point on the tensor core where tensor memory allows: per group an
-    // 8-column tile holding -(128 + z) in every column of the row, and one
-    // more MMA per K step; otherwise q - z is formed on the CUDA cores.
-    static constexpr bool kZtc = (kNB * (kACols + 8) + 15) / 16 * 16 + kNB * kN <= kTmemCols;
-    static constexpr uint32_t kColA = 0;                        // kNB A tiles
-    static constexpr uint32_t kColZ = kNB * kACols;             // kNB zero-point tiles
-    static constexpr uint32_t kColD = (kColZ + (kZtc ? kNB * 8 : 0) + 15) / 16 * 16;  // accumulators
-    static_assert(kColD + kNB * kN <= kTmemCols, "tensor memory budget");
-    static_assert(kColD % 16 == 0, "accumulators 16-column aligned");
+    // Tensor memory: kNA batch slots of A tiles (plus zero-point tiles when
+    // the zero point goes on the tensor core) and kND batch slots of fp32
+    // accumulators, the largest plan that fits in 512 columns.
+    static constexpr int kPlan = tmem_plan(kR0, kACols, kN, int(kTmemCols));
+    static constexpr bool kZtc = kPlan / 100 != 0;
+    static constexpr int kNA = (kPlan / 10) % 10;
+    static constexpr int kND = kPlan % 10;
+    static constexpr uint32_t kColA = 0;                                        // [kNA][kR0][kACols]
+    static constexpr uint32_t kColZ = kNA * kR0 * kACols;                       // [kNA][kR0][8]
+    static constexpr uint32_t kColD = round_up_tc(kColZ + (kZtc ? kNA * kR0 * 8 : 0), 16);  // [kND][kR0][16]
+    static_assert(kPlan > 0, "no tensor-memory plan fits");
+    static_assert(kColD + kND * kR0 * kN <= kTmemCols, "tensor memory budget");
+    static_assert(kPairsW == 8 || kPairsW == 16 || kPairsW == 32, "tcgen05.st width");
+    static_assert(kEW <= kCountersPerTile, "one split-K counter per epilogue warp");
+    static_assert(kR0 >= 1 && kGPS - kR0 >= 1, "two non-empty batches");
 };
 
 // Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B bf16
@@ -104,7 +142,8 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
            (static_cast<uint64_t>(2) << 61);
 }
 
-// Scale / zero point of the GPS groups of one stage for one row.
+// Scales (bf16 pairs) and zero points (byte quads) of the GPS groups of one
+// stage for one row.
 template <int GPS>
 struct RowMeta {
     static constexpr int kS = (GPS + 1) / 2;
@@ -119,40 +158,47 @@ struct RowMeta {
         for (int j = 0; j < kZ; ++j) z[j] = 0;
         if (n >= a.N) return;
         const long long base = static_cast<long long>(n) * a.ng + g0;
-        if (vec) {
-            const uint16_t* sp = a.scales + base;
-            const uint8_t* zp = a.zeros + base;
-            if (GPS == 2) {
-                s[0] = __ldg(reinterpret_cast<const uint32_t*>(sp));
-                z[0] = __ldg(reinterpret_cast<const uint16_t*>(zp));
-            } else if (GPS == 4) {
-                const uint2 v = __ldg(reinterpret_cast<const uint2*>(sp));
-                s[0] = v.x; s[kS > 1 ? 1 : 0] = v.y;
-                z[0] = __ldg(reinterpret_cast<const uint32_t*>(zp));
-            } else if (GPS == 8) {
-                const uint4 v = __ldg(reinterpret_cast<const uint4*>(sp));
-                s[0] = v.x; s[kS > 1 ? 1 : 0] = v.y; s[kS > 2 ? 2 : 0] = v.z; s[kS > 3 ? 3 : 0] = v.w;
-                const uint2 w = __ldg(reinterpret_cast<const uint2*>(zp));
-                z[0] = w.x; z[kZ > 1 ? 1 : 0] = w.y;
-            } else {
+        if constexpr (GPS == 4 || GPS == 8 || GPS == 16) {
+            if (vec) {
+                const uint16_t* sp = a.scales + base;
+                const uint8_t* zp = a.zeros + base;
+                if constexpr (GPS == 4) {
+                    const uint2 v = __ldg(reinterpret_cast<const uint2*>(sp));
+                    s[0] = v.x;
+                    s[1] = v.y;
+                    z[0] = __ldg(reinterpret_cast<const uint32_t*>(zp));
+                } else if constexpr (GPS == 8) {
+                    const uint4 v = __ldg(reinterpret_cast<const uint4*>(sp));
+                    s[0] = v.x;
+                    s[1] = v.y;
+                    s[2] = v.z;
+                    s[3] = v.w;
+                    const uint2 w = __ldg(reinterpret_cast<const uint2*>(zp));
+                    z[0] = w.x;
+                    z[1] = w.y;
+                } else {
 #pragma unroll
-                for (int j = 0; j < kS / 4; ++j) {
-                    const uint4 v = __ldg(reinterpret_cast<const uint4*>(sp) + j);
-                    s[4 * j] = v.x; s[4 * j + 1] = v.y; s[4 * j + 2] = v.z; s[4 * j + 3] = v.w;
+                    for (int j = 0; j < 2; ++j) {
+                        const uint4 v = __ldg(reinterpret_cast<const uint4*>(sp) + j);
+                        s[4 * j] = v.x;
+                        s[4 * j + 1] = v.y;
+                        s[4 * j + 2] = v.z;
+                        s[4 * j + 3] = v.w;
+                    }
+                    const uint4 w = __ldg(reinterpret_cast<const uint4*>(zp));
+                    z[0] = w.x;
+                    z[1] = w.y;
+                    z[2] = w.z;
+                    z[3] = w.w;
                 }
-#pragma unroll
-                for (int j = 0; j < kZ / 4; ++j) {
-                    const uint4 v = __ldg(reinterpret_cast<const uint4*>(zp) + j);
-                    z[4 * j] = v.x; z[4 * j + 1] = v.y; z[4 * j + 2] = v.z; z[4 * j + 3] = v.w;
-                }
+                return;
             }
-        } else {
+        }
 #pragma unroll
-            for (int gi = 0; gi < GPS; ++gi) {
-                if (g0 + gi < a.ng) {
-                    s[gi / 2] |= static_cast<uint32_t>(__ldg(a.scales + base + gi)) << (16 * (gi & 1));
-                    z[gi / 4] |= static_cast<uint32_t>(__ldg(a.zeros + base + gi)) << (8 * (gi & 3));
-                }
+        for (int gi = 0; gi < GPS; ++gi) {
+            if (g0 + gi < a.ng) {
+                s[gi / 2] |= static_cast<uint32_t>(__ldg(a.scales + base + gi)) << (16 * (gi & 1));
+                z[gi / 4] |= static_cast<uint32_t>(__ldg(a.zeros + base + gi)) << (8 * (gi & 3));
             }
         }
     }
@@ -171,46 +217,34 @@ struct RowMeta {
     }
 };
 
-// bf16x2 (128 + lo, 128 + hi) from the low nibble (or 2-bit field, per
-// `mask`) of bytes `sel`-picked from two words.
-__device__ __forceinline__ uint32_t magic_bytes(uint32_t a, uint32_t b, uint32_t sel, uint32_t mask) {
-    return lop3_and_or(__byte_perm(a, b, sel), mask, 0x43004300u);
+// Store NC consecutive 32-bit TMEM columns of the warp's 32 lanes.
+template <int NC>
+__device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t (&v)[NC]);
+template <>
+__device__ __forceinline__ void tmem_st_cols<8>(uint32_t taddr, const uint32_t (&v)[8]) {
+    tmem_st8(taddr, v);
 }
-
-// Optional exact bf16x2 subtraction of zz = (128 + z, 128 + z).
-template <bool SUB>
-__device__ __forceinline__ uint32_t minus_zero(uint32_t v, uint32_t zz) {
-    return SUB ? bf16x2_sub(v, zz) : v;
+template <>
+__device__ __forceinline__ void tmem_st_cols<16>(uint32_t taddr, const uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+        "%13,%14,%15,%16};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+        "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+        : "memory");
 }
-
-// Eight bf16x2 registers (k = 0..15 in natural order) from two 4-bit words:
-// q - z if SUB, else 128 + q.
-template <bool SUB>
-__device__ __forceinline__ void unpack4_k16(uint32_t w0, uint32_t w1, uint32_t zz, uint32_t (&p)[8]) {
-    const uint32_t v0 = w0 >> 4, v1 = w1 >> 4;
-    p[0] = minus_zero<SUB>(magic_bytes(w0, v0, 0x4400u, 0x000f000fu), zz);
-    p[1] = minus_zero<SUB>(magic_bytes(w0, v0, 0x5511u, 0x000f000fu), zz);
-    p[2] = minus_zero<SUB>(magic_bytes(w0, v0, 0x6622u, 0x000f000fu), zz);
-    p[3] = minus_zero<SUB>(magic_bytes(w0, v0, 0x7733u, 0x000f000fu), zz);
-    p[4] = minus_zero<SUB>(magic_bytes(w1, v1, 0x4400u, 0x000f000fu), zz);
-    p[5] = minus_zero<SUB>(magic_bytes(w1, v1, 0x5511u, 0x000f000fu), zz);
-    p[6] = minus_zero<SUB>(magic_bytes(w1, v1, 0x6622u, 0x000f000fu), zz);
-    p[7] = minus_zero<SUB>(magic_bytes(w1, v1, 0x7733u, 0x000f000fu), zz);
-}
-
-// Eight bf16x2 registers (k = 0..15 in natural order) from one 2-bit word:
-// q - z if SUB, else 128 + q.
-template <bool SUB>
-__device__ __forceinline__ void unpack2_k16(uint32_t w, uint32_t zz, uint32_t (&p)[8]) {
-    const uint32_t u1 = w >> 2, u2 = w >> 4, u3 = w >> 6;
-    p[0] = minus_zero<SUB>(magic_bytes(w, u1, 0x4400u, 0x00030003u), zz);
-    p[1] = minus_zero<SUB>(magic_bytes(u2, u3, 0x4400u, 0x00030003u), zz);
-    p[2] = minus_zero<SUB>(magic_bytes(w, u1, 0x5511u, 0x00030003u), zz);
-    p[3] = minus_zero<SUB>(magic_bytes(u2, u3, 0x5511u, 0x00030003u), zz);
-    p[4] = minus_zero<SUB>(magic_bytes(w, u1, 0x6622u, 0x00030003u), zz);
-    p[5] = minus_zero<SUB>(magic_bytes(u2, u3, 0x6622u, 0x00030003u), zz);
-    p[6] = minus_zero<SUB>(magic_bytes(w, u1, 0x7733u, 0x00030003u), zz);
-    p[7] = minus_zero<SUB>(magic_bytes(u2, u3, 0x7733u, 0x00030003u), zz);
+template <>
+__device__ __forceinline__ void tmem_st_cols<32>(uint32_t taddr, const uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+        "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(
+            taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+        "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]),
+        "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]),
+        "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]),
+        "r"(v[30]), "r"(v[31])
+        : "memory");
 }
 
 __device__ __forceinline__ void record_error_tc(const GemmArgs& a, volatile int* abort_flag) {
@@ -218,82 +252,421 @@ __device__ __forceinline__ void record_error_tc(const GemmArgs& a, volatile int*
     atomicExch(a.err, 1);
 }
 
-// NW consecutive packed words starting at word `wi0` of a 128-byte-swizzled row.
-template <int NW>
-__device__ __forceinline__ void load_words(const uint8_t* row, int wi0, int r, uint32_t (&w)[NW]) {
-    const int sw = r & 7;
-    if (NW >= 4) {
-#pragma unroll
-        for (int j = 0; j < NW / 4; ++j) {
-            const int chunk = wi0 / 4 + j;
-            const uint4 v = *reinterpret_cast<const uint4*>(row + ((chunk ^ sw) << 4));
-            w[4 * j] = v.x; w[4 * j + 1] = v.y; w[4 * j + 2] = v.z; w[4 * j + 3] = v.w;
-        }
-    } else if (NW == 2) {
-        const uint2 v = *reinterpret_cast<const uint2*>(row + (((wi0 / 4) ^ sw) << 4) + (wi0 & 3) * 4);
-        w[0] = v.x; w[NW > 1 ? 1 : 0] = v.y;
-    } else {
-        w[0] = *reinterpret_cast<const uint32_t*>(row + (((wi0 / 4) ^ sw) << 4) + (wi0 & 3) * 4);
+// Warp-uniform bounded wait: true only if every lane saw the phase complete.
+__device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+    return __all_sync(kFull, mbar_wait(bar, parity, abort_flag));
+}
+
+// Which packed words of its row a consumer thread reads for one group: the
+// bf16 pairs [p0, p0 + kPairsW) of the stage row (pair p = codes 2p, 2p + 1)
+// live in words [p0 / kPpw, (p0 + kPairsW - 1) / kPpw].  They are fetched as
+// one 8-byte load when they sit in one aligned word pair, else as whole
+// 16-byte chunks.
+template <int BITS, int G, int H, int GI>
+struct WordPlan {
+    using L = Lay<BITS, G>;
+    static constexpr int kP0 = GI * (G / 2) + H * L::kPairsW;
+    static constexpr int kWLo = kP0 / L::kPpw;
+    static constexpr int kWHi = (kP0 + L::kPairsW - 1) / L::kPpw;
+    static constexpr bool kPair = (kWLo / 2) == (kWHi / 2);
+    static constexpr int kBase = kPair ? (kWLo / 2) * 2 : (kWLo / 4) * 4;  // first word loaded
+    static constexpr int kChunks = kPair ? 0 : kWHi / 4 - kWLo / 4 + 1;
+    static constexpr int kNW = kPair ? 2 : 4 * kChunks;                     // words loaded
+};
+
+// Calls f(std::integral_constant<int, I>) for I = B .. E - 1.
+template <int B, int E, class F>
+__device__ __forceinline__ void static_for(F&& f) {
+    if constexpr (B < E) {
+        f(std::integral_constant<int, B>{});
+        static_for<B + 1, E>(f);
     }
 }
 
-// Segment end for one thread (row r, columns C h .. C h + C - 1): store Y, or
-// publish the partial and let the last CTA of the tile sum all partials in k
-// order.  NCT = consumer threads (named barrier 1).
-template <int C, int NCT>
-__device__ __forceinline__ void finish_tile(const GemmArgs& a, const float (&acc)[C], int t,
-                                           bool whole, long long u_lo, int r, int h, int tid,
-                                           bool dead, volatile int* abort_flag,
-                                           volatile int* last_flag) {
+// Unpack group GI's K part H for one row and store it as columns
+// [H kPairsW, (H + 1) kPairsW) of the group's A tile, with H known at compile
+// time (3-bit words do not line up with K steps, so each part has its own
+// word pattern).
+//   row_sw: shared address of the row inside the stage, with the row's
+//           swizzle pattern (row % 8) << 4 already XOR-ed in;
+//   tA:     TMEM address of the group's A tile in the warp's lane quarter.
+template <int BITS, int G, int H, int GI>
+__device__ __forceinline__ void write_group(uint32_t row_sw, uint32_t tA,
+                                            const RowMeta<Lay<BITS, G>::kGPS>& m) {
+    using L = Lay<BITS, G>;
+    using P = WordPlan<BITS, G, H, GI>;
+    uint32_t w[P::kNW];
+    if constexpr (P::kPair) {
+        constexpr int c = P::kBase / 4;  // 16-byte chunk of the stage row
+        constexpr uint32_t box = static_cast<uint32_t>(c / 8) * L::kBoxBytes;
+        const uint2 v = lds64(((row_sw + box) ^ static_cast<uint32_t>((c % 8) << 4)) +
+                              static_cast<uint32_t>((P::kBase % 4) * 4));
+        w[0] = v.x;
+        w[1] = v.y;
+    } else {
+#pragma unroll
+        for (int j = 0; j < P::kChunks; ++j) {
+            const int c = P::kBase / 4 + j;
+            const uint32_t box = static_cast<uint32_t>(c / 8) * L::kBoxBytes;
+            const uint4 v = lds128((row_sw + box) ^ static_cast<uint32_t>((c % 8) << 4));
+            w[4 * j] = v.x;
+            w[4 * j + 1] = v.y;
+            w[4 * j + 2] = v.z;
+            w[4 * j + 3] = v.w;
+        }
+    }
+    constexpr uint32_t kMask = ((1u << BITS) - 1u) * 0x00010001u;
+    const uint32_t zz = L::kZtc ? 0u : m.zero_point(GI);
+    // stores of kStoreCols columns, each issued as soon as its pairs are ready
+    constexpr int kStW = L::kPairsW < kStoreCols ? L::kPairsW : kStoreCols;
+#pragma unroll
+    for (int c = 0; c < L::kPairsW / kStW; ++c) {
+        uint32_t p[kStW];
+#pragma unroll
+        for (int j = 0; j < kStW; ++j) {
+            const int pp = P::kP0 + c * kStW + j;  // pair index in the stage row
+            const int wi = pp / L::kPpw - P::kBase;
+            const int sh = (pp % L::kPpw) * BITS;
+            const uint32_t v = sh ? (w[wi] >> sh) : w[wi];
+            p[j] = lop3_and_or(v, kMask, 0x43004300u);  // (128 + q_2pp, 128 + q_2pp+1)
+            if constexpr (!L::kZtc) p[j] = bf16x2_sub(p[j], zz);
+        }
+        tmem_st_cols<kStW>(tA + H * L::kPairsW + c * kStW, p);
+    }
+}
+
+// The same for 2- and 4-bit codes with the K part h known only at run time:
+// each part covers a whole number of words, so all parts share one word
+// pattern and one copy of the code.
+template <int BITS, int G, int GI>
+__device__ __forceinline__ void write_group_rt(uint32_t row_sw, uint32_t tA,
+                                               const RowMeta<Lay<BITS, G>::kGPS>& m, int h) {
+    using L = Lay<BITS, G>;
+    constexpr int kWG = (G / 2) / L::kPpw;     // words per group
+    constexpr int kWW = L::kPairsW / L::kPpw;  // words per K part
+    static_assert(kWG * L::kPpw == G / 2 && kWW * L::kPpw == L::kPairsW, "whole words per part");
+    const int w0 = GI * kWG + h * kWW;         // first word of the part (a multiple of kWW)
+    uint32_t w[kWW];
+    if constexpr (kWW >= 4) {
+#pragma unroll
+        for (int j = 0; j < kWW / 4; ++j) {
+            const uint32_t c = static_cast<uint32_t>(w0 >> 2) + j;  // 16-byte chunk of the stage row
+            const uint4 v = lds128((row_sw + (c >> 3) * L::kBoxBytes) ^ ((c & 7u) << 4));
+            w[4 * j] = v.x;
+            w[4 * j + 1] = v.y;
+            w[4 * j + 2] = v.z;
+            w[4 * j + 3] = v.w;
+        }
+    } else {
+        const uint32_t c = static_cast<uint32_t>(w0 >> 2);
+        const uint32_t addr = ((row_sw + (c >> 3) * L::kBoxBytes) ^ ((c & 7u) << 4)) +
+                              static_cast<uint32_t>(w0 & 3) * 4u;
+        if constexpr (kWW == 2) {
+            const uint2 v = lds64(addr);
+            w[0] = v.x;
+            w[kWW > 1 ? 1 : 0] = v.y;
+        } else {
+            w[0] = lds32(addr);
+        }
+    }
+    constexpr uint32_t kMask = ((1u << BITS) - 1u) * 0x00010001u;
+    const uint32_t zz = L::kZtc ? 0u : m.zero_point(GI);
+    // stores of kStoreCols columns, each issued as soon as its pairs are ready
+    constexpr int kStW = L::kPairsW < kStoreCols ? L::kPairsW : kStoreCols;
+#pragma unroll
+    for (int c = 0; c < L::kPairsW / kStW; ++c) {
+        uint32_t p[kStW];
+#pragma unroll
+        for (int j = 0; j < kStW; ++j) {
+            const int i = c * kStW + j;
+            const int sh = (i % L::kPpw) * BITS;
+            const uint32_t v = sh ? (w[i / L::kPpw] >> sh) : w[i / L::kPpw];
+            p[j] = lop3_and_or(v, kMask, 0x43004300u);  // (128 + q_2i, 128 + q_2i+1)
+            if constexpr (!L::kZtc) p[j] = bf16x2_sub(p[j], zz);
+        }
+        tmem_st_cols<kStW>(tA + h * L::kPairsW + c * kStW, p);
+    }
+}
+
+// End of a tile segment for one epilogue warp (rows 32 q + lane, all
+// accumulator columns): store Y, or publish the partial sums and let the
+// warp of the last CTA to finish the tile add all partials in k order.  Each
+// (tile, lane quarter) pair has its own arrival counter, so warps never wait
+// for one another.
+__device__ __forceinline__ void finish_rows(const GemmArgs& a, const float (&acc)[kN], int t,
+                                            bool whole, long long u_lo, int r, int q, int lane) {
     const int n = t * kBN + r;
     if (whole) {
-        if (!dead && n < a.N)
+        if (n < a.N)
 #pragma unroll
-            for (int j = 0; j < C; ++j)
-                if (C * h + j < a.M) a.y[static_cast<size_t>(C * h + j) * a.N + n] = acc[j];
+            for (int j = 0; j < kN; ++j)
+                if (j < a.M) a.y[static_cast<size_t>(j) * a.N + n] = acc[j];
         return;
     }
     const int t_first = static_cast<int>(u_lo / a.I);
     float* mine = a.partials + static_cast<size_t>(2 * blockIdx.x + (t == t_first ? 0 : 1)) *
                                    (kMaxCols * kBN);
 #pragma unroll
-    for (int j = 0; j < C; ++j) __stcg(mine + (C * h + j) * kBN + r, acc[j]);
-    named_bar_sync(1, NCT);
+    for (int j = 0; j < kN; ++j)
+        if (j < a.M) __stcg(mine + j * kBN + r, acc[j]);
+    // The warp barrier orders every lane's partial before lane 0's release
+    // (acq_rel) increment; the reading warp's lane 0 acquires it and the next
+    // warp barrier orders the other lanes' reads after that acquire.
+    __syncwarp();
     const long long tu0 = static_cast<long long>(t) * a.I;
     const int b_first = static_cast<int>(((tu0 + 1) * a.P + a.U - 1) / a.U - 1);
     const int b_last = static_cast<int>(((tu0 + a.I) * a.P + a.U - 1) / a.U - 1);
-    if (tid == 0) {
-        if (*abort_flag) {
-            *last_flag = 0;
+    int* ctr = a.counters + static_cast<size_t>(t) * kCountersPerTile + q;
+    int last = 0;
+    if (lane == 0) last = (atomic_add_acq_rel_gpu(ctr, 1) == b_last - b_first) ? 1 : 0;
+    last = __shfl_sync(kFull, last, 0);
+    if (!last) return;
+    float tot[kN];
+#pragma unroll
+    for (int j = 0; j < kN; ++j) tot[j] = 0.f;
+    for (int b = b_first; b <= b_last; ++b) {
+        if (b == static_cast<int>(blockIdx.x)) {
+#pragma unroll
+            for (int j = 0; j < kN; ++j) tot[j] += acc[j];
         } else {
-            const int prev = atomic_add_acq_rel_gpu(a.counters + t, 1);
-            *last_flag = (prev == b_last - b_first) ? 1 : 0;
+            const int tb = static_cast<int>((a.U * b / a.P) / a.I);
+            const float* src =
+                a.partials + static_cast<size_t>(2 * b + (t == tb ? 0 : 1)) * (kMaxCols * kBN);
+#pragma unroll
+            for (int j = 0; j < kN; ++j)
+                if (j < a.M) tot[j] += __ldcg(src + j * kBN + r);
         }
     }
-    named_bar_sync(1, NCT);
-    if (*last_flag) {
-        float tot[C];
+    if (n < a.N)
 #pragma unroll
-        for (int j = 0; j < C; ++j) tot[j] = 0.f;
-        for (int b = b_first; b <= b_last; ++b) {
-            if (b == static_cast<int>(blockIdx.x)) {
-#pragma unroll
-                for (int j = 0; j < C; ++j) tot[j] += acc[j];
-            } else {
-                const int tb = static_cast<int>((a.U * b / a.P) / a.I);
-                const float* src = a.partials +
-                                   static_cast<size_t>(2 * b + (t == tb ? 0 : 1)) * (kMaxCols * kBN);
-#pragma unroll
-                for (int j = 0; j < C; ++j) tot[j] += __ldcg(src + (C * h + j) * kBN + r);
+        for (int j = 0; j < kN; ++j)
+            if (j < a.M) a.y[static_cast<size_t>(j) * a.N + n] = tot[j];
+    if (lane == 0) *ctr = 0;
+}
+
+// Shared-memory barriers of one CTA.
+template <int S, int NA, int ND>
+struct Bars {
+    uint64_t full[S];    // stage landed (TMA transaction bytes)
+    uint64_t empty[S];   // stage consumed: unpack warps + one MMA commit
+    uint64_t filled[NA]; // A slot written (unpack warps, and epilogue warps for zero-point tiles)
+    uint64_t afree[NA];  // A slot's MMAs complete (tcgen05.commit)
+    uint64_t dfull[ND];  // accumulator slot's MMAs complete (tcgen05.commit)
+    uint64_t dfree[ND];  // accumulator slot read back (epilogue warps)
+    uint64_t drain;      // every MMA complete
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+// Ring position: slot index and phase parity of a barrier ring of N entries.
+template <int N>
+struct Ring {
+    uint32_t slot = 0, phase = 0;
+    __device__ __forceinline__ void next() {
+        if (++slot == N) {
+            slot = 0;
+            phase ^= 1u;
+        }
+    }
+};
+
+// Unpack warp: turns the stage's packed words into A tiles, batch by batch.
+// HT is the warp's K part when fixed at compile time, -1 when read at run time.
+template <int BITS, int G, int HT, class B>
+__device__ __forceinline__ void unpack_warp(const GemmArgs& a, uint32_t smem_u32, B& bars,
+                                            uint32_t tmem, volatile int* abort_flag, int warp,
+                                            int lane, int n_units, int t_first, int i_first) {
+    using L = Lay<BITS, G>;
+    using RM = RowMeta<L::kGPS>;
+    const int h = HT >= 0 ? HT : (warp >> 2);
+    const int q = warp & 3;
+    const int r = 32 * q + lane;                                       // tile row == TMEM lane
+    const uint32_t tl = tmem + (static_cast<uint32_t>(32 * q) << 16);  // lane quarter
+    const uint32_t row_off = static_cast<uint32_t>(r * 128) | (static_cast<uint32_t>(lane & 7) << 4);
+    const bool vec = a.meta_vec != 0;
+    bool dead = false;  // after a failed wait: no more shared or tensor memory work
+
+    // Zero points are needed here only when they are subtracted on the CUDA
+    // cores; otherwise the epilogue warps write the zero-point tiles.
+    int ft = t_first, fi = i_first;
+    auto fetch = [&](RM& m) {
+        if constexpr (!L::kZtc) {
+            m.load(a, ft * kBN + r, static_cast<long long>(fi) * L::kGPS, vec);
+            if (++fi == a.I) {
+                fi = 0;
+                ++ft;
             }
         }
-        if (n < a.N)
-#pragma unroll
-            for (int j = 0; j < C; ++j)
-                if (C * h + j < a.M) a.y[static_cast<size_t>(C * h + j) * a.N + n] = tot[j];
-        if (tid == 0) a.counters[t] = 0;
+    };
+    auto fail = [&]() {
+        record_error_tc(a, abort_flag);
+        dead = true;
+    };
+
+    Ring<L::kStages> st;
+    Ring<L::kNA> as;
+    RM cur, nxt;
+    if (n_units > 0) fetch(cur);
+    for (int k = 0; k < n_units; ++k) {
+        if (k + 1 < n_units) fetch(nxt);
+        if (!dead && !wait_all(&bars.full[st.slot], st.phase, abort_flag)) fail();
+        // Both A slots of this stage must have left the tensor core: the MMAs
+        // complete in order, so waiting for the later slot's previous batch
+        // covers the earlier one.
+        Ring<L::kNA> as1 = as;
+        as1.next();
+        if (!dead && !wait_all(&bars.afree[as1.slot], as1.phase ^ 1u, abort_flag)) fail();
+        const uint32_t row_sw = smem_u32 + st.slot * L::kStageBytes + row_off;
+        static_for<0, 2>([&](auto bc) {
+            constexpr int BB = decltype(bc)::value;
+            constexpr int g_lo = BB == 0 ? 0 : L::kR0;
+            constexpr int g_hi = BB == 0 ? L::kR0 : L::kGPS;
+            if (!dead) {
+                const uint32_t slot_col = as.slot * (L::kR0 * L::kACols);
+                static_for<g_lo, g_hi>([&](auto gc) {
+                    constexpr int GI = decltype(gc)::value;
+                    const uint32_t tA = tl + L::kColA + slot_col + (GI - g_lo) * L::kACols;
+                    if constexpr (HT >= 0)
+                        write_group<BITS, G, HT, GI>(row_sw, tA, cur);
+                    else
+                        write_group_rt<BITS, G, GI>(row_sw, tA, cur, h);
+                });
+                tmem_wait_st();
+                tc_fence_before();
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars.filled[as.slot]);
+            as.next();
+        });
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars.empty[st.slot]);  // the stage's words are no longer needed
+        cur = nxt;
+        st.next();
     }
-    named_bar_sync(1, NCT);
+}
+
+// Epilogue warp (lane quarter q).  Per batch j of the CTA's schedule it
+// writes batch j's zero-point tiles (when the zero point is applied on the
+// tensor core), then reads batch j - 1's accumulators back, adds scale * D to
+// the row's 16 fp32 sums and ends tile segments.
+template <int BITS, int G, class B>
+__device__ __forceinline__ void epilogue_warp(const GemmArgs& a, B& bars, uint32_t tmem,
+                                              volatile int* abort_flag, int q, int lane,
+                                              long long u_lo, int n_units, int t_first,
+                                              int i_first) {
+    using L = Lay<BITS, G>;
+    using RM = RowMeta<L::kGPS>;
+    const int r = 32 * q + lane;
+    const uint32_t tl = tmem + (static_cast<uint32_t>(32 * q) << 16);
+    const bool vec = a.meta_vec != 0;
+    bool dead = false;
+    float acc[kN];
+#pragma unroll
+    for (int j = 0; j < kN; ++j) acc[j] = 0.f;
+    auto fail = [&]() {
+        record_error_tc(a, abort_flag);
+        dead = true;
+    };
+
+    int ft = t_first, fi = i_first;  // unit whose scales and zero points are fetched next
+    auto fetch = [&](RM& m) {
+        m.load(a, ft * kBN + r, static_cast<long long>(fi) * L::kGPS, vec);
+        if (++fi == a.I) {
+            fi = 0;
+            ++ft;
+        }
+    };
+    Ring<L::kNA> as;
+    Ring<L::kND> ds;
+    // Zero-point tiles of one batch of the current unit into A slot `as`.
+    auto write_z = [&](auto bc, const RM& m) {
+        constexpr int BB = decltype(bc)::value;
+        constexpr int g_lo = BB == 0 ? 0 : L::kR0;
+        constexpr int g_hi = BB == 0 ? L::kR0 : L::kGPS;
+        if constexpr (L::kZtc) {
+            if (!dead && !wait_all(&bars.afree[as.slot], as.phase ^ 1u, abort_flag)) fail();
+            if (!dead) {
+                static_for<g_lo, g_hi>([&](auto gc) {
+                    constexpr int GI = decltype(gc)::value;
+                    tmem_st8_same(tl + L::kColZ + (as.slot * L::kR0 + (GI - g_lo)) * 8,
+                                  m.neg_zero_point(GI));
+                });
+                tmem_wait_st();
+                tc_fence_before();
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars.filled[as.slot]);
+        }
+        as.next();
+    };
+    // Accumulators of one batch (scales from m) into acc.
+    auto read_d = [&](auto bc, const RM& m) {
+        constexpr int BB = decltype(bc)::value;
+        constexpr int g_lo = BB == 0 ? 0 : L::kR0;
+        constexpr int g_hi = BB == 0 ? L::kR0 : L::kGPS;
+        if (!dead && !wait_all(&bars.dfull[ds.slot], ds.phase, abort_flag)) fail();
+        if (!dead) {
+            tc_fence_after();
+            // two groups' accumulators at a time keep the registers in bounds
+            static_for<0, (g_hi - g_lo + 1) / 2>([&](auto pc) {
+                constexpr int G0 = g_lo + 2 * decltype(pc)::value;
+                constexpr int NG = (G0 + 1 < g_hi) ? 2 : 1;
+                uint32_t v[NG][kN];
+                static_for<0, NG>([&](auto gc) {
+                    constexpr int J = decltype(gc)::value;
+                    tmem_ld16(tl + L::kColD + (ds.slot * L::kR0 + (G0 + J - g_lo)) * kN, v[J]);
+                });
+                tmem_wait_ld();
+                static_for<0, NG>([&](auto gc) {
+                    constexpr int J = decltype(gc)::value;
+                    const float sc = m.scale(G0 + J);
+#pragma unroll
+                    for (int j = 0; j < kN; ++j) acc[j] = fmaf(sc, __uint_as_float(v[J][j]), acc[j]);
+                });
+            });
+            tc_fence_before();
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars.dfree[ds.slot]);
+        ds.next();
+    };
+    auto finish = [&](int tt, bool whole) {
+        if (!dead) finish_rows(a, acc, tt, whole, u_lo, r, q, lane);
+#pragma unroll
+        for (int j = 0; j < kN; ++j) acc[j] = 0.f;
+    };
+
+    constexpr std::integral_constant<int, 0> kB0{};
+    constexpr std::integral_constant<int, 1> kB1{};
+    RM cur, nxt, prev;
+    if (n_units > 0) fetch(cur);
+    int t = t_first, i = i_first;
+    int prev_t = 0;
+    bool prev_end = false, prev_whole = false;
+    for (int k = 0; k < n_units; ++k) {
+        if (k + 1 < n_units) fetch(nxt);
+        write_z(kB0, cur);
+        if (k > 0) {
+            read_d(kB1, prev);  // the previous unit's second batch
+            if (prev_end) finish(prev_t, prev_whole);
+        }
+        write_z(kB1, cur);
+        read_d(kB0, cur);
+        prev = cur;
+        prev_t = t;
+        prev_end = (i == a.I - 1) || (k == n_units - 1);
+        prev_whole = (i == a.I - 1) && (t != t_first || i_first == 0);
+        if (++i == a.I) {
+            i = 0;
+            ++t;
+        }
+        cur = nxt;
+    }
+    if (n_units > 0) {
+        read_d(kB1, prev);
+        finish(prev_t, prev_whole);
+    }
+    tc_fence_before();
 }
 
 template <int BITS, int G>
@@ -302,47 +675,49 @@ __global__ void __launch_bounds__(Lay<BITS, G>::kThreads, 1)
                    const GemmArgs a) {
     using L = Lay<BITS, G>;
     constexpr int S = L::kStages;
+    using BarsT = Bars<S, L::kNA, L::kND>;
+    static_assert(sizeof(BarsT) <= 512, "barrier block");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBarOffset);
-    uint64_t* empty = full + S;
-    uint64_t* filled = empty + S;        // slot's A tile written (8 consumer warps)
-    uint64_t* done = filled + L::kNB;    // slot's MMAs complete (tcgen05.commit)
-    uint64_t* drain = done + L::kNB;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    volatile int* last_flag = abort_flag + 1;
+    const uint32_t smem_u32 = smem_addr(smem);
+    BarsT& bars = *reinterpret_cast<BarsT*>(smem + L::kBarOffset);
+    volatile int* abort_flag = &bars.abort_flag;
 
-    const int warp = threadIdx.x >> 5;
+    // warp index through a shuffle so that the compiler treats it as uniform
+    const int warp = __shfl_sync(kFull, static_cast<int>(threadIdx.x >> 5), 0);
     const int lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        for (int i = 0; i < S; ++i) {
-            mbar_init(&full[i], 1);
-            mbar_init(&empty[i], L::kCW + 1);  // consumers read W, MMAs read X
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&bars.full[s], 1);
+            mbar_init(&bars.empty[s], L::kUW + 1);
         }
-        for (int i = 0; i < L::kNB; ++i) {
-            mbar_init(&filled[i], L::kCW);
-            mbar_init(&done[i], 1);
+        for (int s = 0; s < L::kNA; ++s) {
+            mbar_init(&bars.filled[s], L::kUW + (L::kZtc ? L::kEW : 0));
+            mbar_init(&bars.afree[s], 1);
         }
-        mbar_init(drain, 1);
+        for (int s = 0; s < L::kND; ++s) {
+            mbar_init(&bars.dfull[s], 1);
+            mbar_init(&bars.dfree[s], L::kEW);
+        }
+        mbar_init(&bars.drain, 1);
         *abort_flag = 0;
-        *last_flag = 0;
         fence_mbar_init();
     }
     if (warp == L::kMmaWarp) {
-        tmem_alloc(smem_addr(tmem_slot), kTmemCols);
+        tmem_alloc(smem_addr(&bars.tmem_base), kTmemCols);
         tmem_relinquish();
         tc_fence_before();
     }
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
+    const uint32_t tmem = bars.tmem_base;
 
     const long long u_lo = a.U * blockIdx.x / a.P;
     const long long u_hi = a.U * (blockIdx.x + 1) / a.P;
     const int n_units = static_cast<int>(u_hi - u_lo);
     const int t_first = static_cast<int>(u_lo / a.I);
     const int i_first = static_cast<int>(u_lo - static_cast<long long>(t_first) * a.I);
+    constexpr uint32_t kTail = 32 * (L::kUW + L::kEW + 1);  // warps that meet before dealloc
 
     if (warp == L::kProducerWarp) {
         // ------------------------------------------------------------ producer
@@ -353,6 +728,7 @@ __global__ void __launch_bounds__(Lay<BITS, G>::kThreads, 1)
         const uint64_t pol_x = policy_evict_last();
         int t = t_first, i = i_first;
         uint32_t it = 0;
+        Ring<S> st;
         bool ok = true;
         for (int k = 0; k < n_units; ++k, ++it) {
             if (k == 0 || i == 0) {
@@ -369,36 +745,37 @@ __global__ void __launch_bounds__(Lay<BITS, G>::kThreads, 1)
                 if (ze16 > zb16)
                     prefetch_l2_bulk(reinterpret_cast<const void*>(zb16), static_cast<uint32_t>(ze16 - zb16));
             }
-            const int slot = static_cast<int>(it % S);
-            if (!mbar_wait(&empty[slot], ((it / S) & 1u) ^ 1u, abort_flag)) {
+            if (!mbar_wait(&bars.empty[st.slot], st.phase ^ 1u, abort_flag)) {
                 record_error_tc(a, abort_flag);
                 ok = false;
                 break;
             }
-            uint8_t* st = smem + slot * L::kStageBytes;
-            mbar_arrive_expect_tx(&full[slot], L::kWBytes + L::kXBytes);
+            uint8_t* stage = smem + st.slot * L::kStageBytes;
+            uint64_t* fb = &bars.full[st.slot];
+            mbar_arrive_expect_tx(fb, L::kWBytes + L::kXBytes);
 #pragma unroll
             for (int b = 0; b < L::kBoxes; ++b)
-                tma_load_2d(st + b * L::kBoxBytes, &tmW, (i * L::kBoxes + b) * kWordsPerStage, t * kBN,
-                            &full[slot], pol_w);
+                tma_load_2d(stage + b * L::kBoxBytes, &tmW, (i * L::kBoxes + b) * kWordsPerStage,
+                            t * kBN, fb, pol_w);
             if (a.x3d) {
-                tma_load_3d(st + L::kWBytes, &tmX, 0, 0, i * L::kXBoxes, &full[slot], pol_x);
+                tma_load_3d(stage + L::kWBytes, &tmX, 0, 0, i * L::kXBoxes, fb, pol_x);
             } else {
 #pragma unroll
                 for (int b = 0; b < L::kXBoxes; ++b)
-                    tma_load_2d(st + L::kWBytes + b * L::kXBoxBytes, &tmX,
-                                i * L::kStageValues + b * L::kXBoxValues, 0, &full[slot], pol_x);
+                    tma_load_2d(stage + L::kWBytes + b * L::kXBoxBytes, &tmX,
+                                i * L::kStageValues + b * L::kXBoxValues, 0, fb, pol_x);
             }
             if (++i == a.I) {
                 i = 0;
                 ++t;
             }
+            st.next();
         }
         if (!ok) {
             // let copies already in flight land before the CTA's shared memory goes away
             const uint32_t first = it > S ? it - S : 0;
             volatile int never = 0;
-            for (uint32_t j = first; j < it; ++j) mbar_wait(&full[j % S], (j / S) & 1u, &never);
+            for (uint32_t j = first; j < it; ++j) mbar_wait(&bars.full[j % S], (j / S) & 1u, &never);
         }
         return;
     }
@@ -407,199 +784,81 @@ __global__ void __launch_bounds__(Lay<BITS, G>::kThreads, 1)
         // --------------------------------------------------------- MMA issuer
         // The whole warp walks the schedule (uniform control flow); one
         // elected lane issues the MMAs and commits.
-        uint32_t gl = 0;
         bool ok = true;
+        Ring<S> st;
+        Ring<L::kNA> as;
+        Ring<L::kND> ds;
         for (int k = 0; k < n_units && ok; ++k) {
-            const int slot = k % S;
-            if (!__all_sync(0xffffffffu, mbar_wait(&full[slot], (static_cast<uint32_t>(k) / S) & 1u,
-                                                   abort_flag))) {
+            if (!wait_all(&bars.full[st.slot], st.phase, abort_flag)) {
                 ok = false;
                 break;
             }
-            const uint64_t desc0 = desc_sw128(smem_addr(smem + slot * L::kStageBytes + L::kWBytes));
-#pragma unroll
-            for (int gi = 0; gi < L::kGPS; ++gi, ++gl) {
-                const uint32_t sb = gl % L::kNB;
-                if (!__all_sync(0xffffffffu, mbar_wait(&filled[sb], (gl / L::kNB) & 1u, abort_flag))) {
+            const uint64_t desc0 = desc_sw128(smem_u32 + st.slot * L::kStageBytes + L::kWBytes);
+            static_for<0, 2>([&](auto bc) {
+                constexpr int BB = decltype(bc)::value;
+                constexpr int g_lo = BB == 0 ? 0 : L::kR0;
+                constexpr int g_hi = BB == 0 ? L::kR0 : L::kGPS;
+                if (!ok) return;
+                if (!wait_all(&bars.filled[as.slot], as.phase, abort_flag) ||
+                    !wait_all(&bars.dfree[ds.slot], ds.phase ^ 1u, abort_flag)) {
                     ok = false;
-                    break;
+                    return;
                 }
                 tc_fence_after();
                 if (elect_one()) {
-                    const uint32_t tA = tmem + L::kColA + sb * L::kACols;
-                    const uint32_t tD = tmem + L::kColD + sb * kN;
+                    static_for<g_lo, g_hi>([&](auto gc) {
+                        constexpr int GI = decltype(gc)::value;
+                        const uint32_t tA = tmem + L::kColA + (as.slot * L::kR0 + (GI - g_lo)) * L::kACols;
+                        const uint32_t tZ = tmem + L::kColZ + (as.slot * L::kR0 + (GI - g_lo)) * 8;
+                        const uint32_t tD = tmem + L::kColD + (ds.slot * L::kR0 + (GI - g_lo)) * kN;
 #pragma unroll
-                    for (int s = 0; s < L::kSteps; ++s) {
-                        const int v0 = gi * G + 16 * s;  // first value of this K step in the stage
-                        const uint64_t bdesc =
-                            desc0 + static_cast<uint64_t>(((v0 / 64) * L::kXBoxBytes + (v0 % 64) * 2) >> 4);
-                        tc_mma_ts(tD, tA + 8 * s, bdesc, kIdesc, s > 0 ? 1u : 0u);
-                        if (L::kZtc) tc_mma_ts(tD, tmem + L::kColZ + sb * 8, bdesc, kIdesc, 1u);
-                    }
-                    tc_commit(&done[sb]);
-                    if (gi == L::kGPS - 1) tc_commit(&empty[slot]);
+                        for (int s = 0; s < L::kSteps; ++s) {
+                            const int v0 = GI * G + 16 * s;  // first value of this K step in the stage
+                            const uint64_t bdesc =
+                                desc0 + static_cast<uint64_t>(((v0 / 64) * L::kXBoxBytes + (v0 % 64) * 2) >> 4);
+                            tc_mma_ts(tD, tA + 8 * s, bdesc, kIdesc, s > 0 ? 1u : 0u);
+                            if constexpr (L::kZtc) tc_mma_ts(tD, tZ, bdesc, kIdesc, 1u);
+                        }
+                    });
+                    tc_commit(&bars.afree[as.slot]);
+                    tc_commit(&bars.dfull[ds.slot]);
+                    if (BB == 1) tc_commit(&bars.empty[st.slot]);
                 }
                 __syncwarp();
-            }
+                as.next();
+                ds.next();
+            });
+            st.next();
         }
         if (!ok && lane == 0) record_error_tc(a, abort_flag);
         // every MMA issued above has completed once `drain` flips
-        if (elect_one()) tc_commit(drain);
+        if (elect_one()) tc_commit(&bars.drain);
         __syncwarp();
         volatile int never = 0;
-        mbar_wait(drain, 0, &never);
-        named_bar_sync(3, 32 * (L::kCW + 1));
+        mbar_wait(&bars.drain, 0, &never);
+        named_bar_sync(3, kTail);
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
         return;
     }
 
-    // ---------------------------------------------------------------- consumers
-    const int tid = threadIdx.x;  // 0 .. 255
-    const int q = warp & 3;       // TMEM lane quarter
-    const int h = warp >> 2;      // which K steps of each group (and columns of D) this warp takes
-    const int r = 32 * q + lane;  // tile row == TMEM lane
-    const uint32_t lane_off = static_cast<uint32_t>(32 * q) << 16;
-    const bool vec = a.meta_vec != 0;
-    // After a failed wait a warp stops touching tensor memory but keeps
-    // arriving on barriers and walking the named barriers of its siblings.
-    bool dead = false;
-    constexpr int C = L::kColsW;
-    float acc[C];
-#pragma unroll
-    for (int j = 0; j < C; ++j) acc[j] = 0.f;
-
-    using RM = RowMeta<L::kGPS>;
-    int t = t_first, i = i_first;    // unit being computed
-    int pt = t_first, pi = i_first;  // unit whose group values are fetched next
-    uint32_t gl = 0;  // groups whose A tiles were written
-    // Scales of the previous stage and that stage's segment bookkeeping: its
-    // second batch is read back during the next stage.
-    uint32_t sprev[RM::kS];
-#pragma unroll
-    for (int j = 0; j < RM::kS; ++j) sprev[j] = 0;
-    int prev_t = 0;
-    bool prev_end = false, prev_whole = false;
-
-    auto fetch = [&](RM& m) {
-        m.load(a, pt * kBN + r, static_cast<long long>(pi) * L::kGPS, vec);
-        if (++pi == a.I) {
-            pi = 0;
-            ++pt;
-        }
-    };
-    auto scale_of = [](const uint32_t* s, int gi) {
-        const uint32_t w = s[gi / 2];
-        return __uint_as_float((gi & 1) ? (w & 0xffff0000u) : (w << 16));
-    };
-    auto finish = [&](int tt, bool wh) {
-        finish_tile<C, 32 * L::kCW>(a, acc, tt, wh, u_lo, r, h, tid, dead, abort_flag, last_flag);
-#pragma unroll
-        for (int j = 0; j < C; ++j) acc[j] = 0.f;
-    };
-    // Read back the accumulators of the kR groups [g0, g0 + kR), whose scales
-    // are s[first .. first + kR), and add scale * D to acc.
-    auto read_batch = [&](uint32_t g0, const uint32_t* s, int first) {
-        const uint32_t glast = g0 + L::kR - 1;  // MMAs complete in order
-        if (!dead && !mbar_wait(&done[glast % L::kNB], (glast / L::kNB) & 1u, abort_flag)) {
-            record_error_tc(a, abort_flag);
-            dead = true;
-        }
-        if (dead) return;
-        tc_fence_after();
-        uint32_t v[L::kR][C];
-#pragma unroll
-        for (int j = 0; j < L::kR; ++j)
-            tmem_ld_cols<C>(tmem + L::kColD + ((g0 + j) % L::kNB) * kN + C * h + lane_off, v[j]);
-        tmem_wait_ld();
-#pragma unroll
-        for (int j = 0; j < L::kR; ++j) {
-            const float sc = scale_of(s, first + j);
-#pragma unroll
-            for (int jj = 0; jj < C; ++jj) acc[jj] = fmaf(sc, __uint_as_float(v[j][jj]), acc[jj]);
-        }
-    };
-    // Unpack and store the A tiles of groups [gb, gb + kR) of the stage.
-    auto write_batch = [&](const RM& m, const uint8_t* row0, int gb) {
-        if (!dead) {
-#pragma unroll
-            for (int j = 0; j < L::kR; ++j) {
-                const int gi = gb + j;
-                const uint32_t sb = (gl + j) % L::kNB;
-                uint32_t w[L::kWordsW];
-                const uint32_t zz = m.zero_point(gi);
-                const int wi = (BITS == 4 ? gi * (G / 8) : gi * (G / 16)) + h * L::kWordsW;
-                load_words<L::kWordsW>(row0 + (wi / kWordsPerStage) * L::kBoxBytes,
-                                       wi % kWordsPerStage, r, w);
-                const uint32_t tA = tmem + L::kColA + sb * L::kACols + lane_off;
-#pragma unroll
-                for (int hs = 0; hs < L::kStepsW; ++hs) {
-                    uint32_t p[8];
-                    if (BITS == 4) {
-                        unpack4_k16<!L::kZtc>(w[2 * hs], w[2 * hs + 1], zz, p);
-                    } else {
-                        unpack2_k16<!L::kZtc>(w[hs], zz, p);
-                    }
-                    tmem_st8(tA + 8 * (h * L::kStepsW + hs), p);
-                }
-                if (L::kZtc && h == 0)
-                    tmem_st8_same(tmem + L::kColZ + sb * 8 + lane_off, m.neg_zero_point(gi));
-            }
-            tmem_wait_st();
-            tc_fence_before();
-        }
-        __syncwarp();
-        if (lane == 0)
-#pragma unroll
-            for (int j = 0; j < L::kR; ++j) mbar_arrive(&filled[(gl + j) % L::kNB]);
-        gl += L::kR;
-    };
-    auto unit = [&](const RM& m, int k) {
-        const int slot = k % S;
-        if (!dead && !mbar_wait(&full[slot], (static_cast<uint32_t>(k) / S) & 1u, abort_flag)) {
-            record_error_tc(a, abort_flag);
-            dead = true;
-        }
-        const uint8_t* row0 = smem + slot * L::kStageBytes + r * 128;
-        // first batch; then the previous stage's second batch is read back
-        write_batch(m, row0, 0);
-        if (k > 0) {
-            read_batch(gl - 2 * L::kR, sprev, L::kR);
-            if (prev_end) finish(prev_t, prev_whole);
-        }
-        // second batch; the stage's words are then no longer needed
-        write_batch(m, row0, L::kR);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[slot]);
-        read_batch(gl - 2 * L::kR, m.s, 0);
-#pragma unroll
-        for (int j = 0; j < RM::kS; ++j) sprev[j] = m.s[j];
-        prev_t = t;
-        prev_end = (i == a.I - 1) || (k == n_units - 1);
-        prev_whole = (i == a.I - 1) && (t != t_first || i_first == 0);
-        if (++i == a.I) {
-            i = 0;
-            ++t;
-        }
-    };
-
-    RM m0, m1;
-    if (n_units > 0) fetch(m0);
-    if (n_units > 1) fetch(m1);
-    for (int k = 0; k < n_units; k += 2) {
-        unit(m0, k);
-        if (k + 2 < n_units) fetch(m0);
-        if (k + 1 < n_units) {
-            unit(m1, k + 1);
-            if (k + 3 < n_units) fetch(m1);
-        }
+    if (warp >= L::kUW) {
+        // ------------------------------------------------------------ epilogue
+        epilogue_warp<BITS, G>(a, bars, tmem, abort_flag, warp & 3, lane, u_lo, n_units, t_first,
+                               i_first);
+    } else if constexpr (BITS == 3) {
+        // ------------------------------------------------------------ unpack
+        static_for<0, L::kSplit>([&](auto hc) {
+            constexpr int H = decltype(hc)::value;
+            if ((warp >> 2) == H)
+                unpack_warp<BITS, G, H>(a, smem_u32, bars, tmem, abort_flag, warp, lane, n_units,
+                                        t_first, i_first);
+        });
+    } else {
+        unpack_warp<BITS, G, -1>(a, smem_u32, bars, tmem, abort_flag, warp, lane, n_units, t_first,
+                                 i_first);
     }
-    if (n_units > 0) {
-        // the last stage's second batch
-        read_batch(gl - L::kR, sprev, L::kR);
-        finish(prev_t, prev_whole);
-    }
-    named_bar_sync(3, 32 * (L::kCW + 1));
+    named_bar_sync(3, kTail);
 }
 
 template <int BITS, int G>

@@ -1,0 +1,14 @@
+// 3-bit instantiations of the tensor-core (tcgen05) GEMM kernel.
+#include "wq_gemm_tc.cuh"
+
+namespace wq {
+
+cudaError_t launch_gemm_tc_b3(int group, const CUtensorMap& tmW, const CUtensorMap& tmX,
+                              const GemmArgs& a, cudaStream_t s) {
+    if (group == 128) return tc::launch_tc<3, 128>(tmW, tmX, a, s);
+    if (group == 64) return tc::launch_tc<3, 64>(tmW, tmX, a, s);
+    if (group == 32) return tc::launch_tc<3, 32>(tmW, tmX, a, s);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace wq

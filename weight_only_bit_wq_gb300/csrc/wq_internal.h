@@ -7,27 +7,30 @@
 
 namespace wq {
 
-constexpr int kConsumerWarps = 8;
-constexpr int kThreads = 32 * (kConsumerWarps + 1);  // + one TMA producer warp
-constexpr int kBN = 16 * kConsumerWarps;             // weight rows per tile
-constexpr int kWordsPerStage = 32;                   // packed words per row per stage (128 B)
-constexpr int kMaxCols = 16;                         // max stacked rows M
-constexpr int kMaxSplit = 8;                         // max CTAs sharing one tile
-constexpr size_t kWsHeader = 256;                    // error word + padding
+constexpr int kBN = 128;              // weight rows per tile (TMEM lanes)
+constexpr int kWordsPerStage = 32;    // packed words per row per TMA box (128 B)
+constexpr int kMaxCols = 16;          // max stacked rows M
+constexpr int kMaxSplit = 8;          // max CTAs sharing one tile
+constexpr int kCountersPerTile = 16;  // split-K arrival counters per tile (one per consumer warp)
+constexpr size_t kWsHeader = 256;     // error word + padding
 
-// Values per packed word and per stage.
+// Values per packed word.
 constexpr int values_per_word(int bits) { return bits == 4 ? 8 : bits == 3 ? 10 : 16; }
-constexpr int stage_values(int bits) { return kWordsPerStage * values_per_word(bits); }
-// The tensor-core kernel reads tc_boxes(bits) adjacent 32-word boxes per row per stage.
-constexpr int tc_boxes(int bits) { return bits == 4 ? 2 : 1; }
-constexpr int tc_stage_values(int bits) { return tc_boxes(bits) * stage_values(bits); }
+// 32-word boxes per row per stage, chosen so that a stage holds whole groups
+// and the per-stage tensor-memory tiles fit in 512 columns.
+constexpr int tc_boxes(int bits, int group) {
+    return bits == 4 ? (group == 32 ? 1 : 2) : bits == 3 ? (group == 128 ? 2 : 1) : 1;
+}
+constexpr int tc_stage_values(int bits, int group) {
+    return tc_boxes(bits, group) * kWordsPerStage * values_per_word(bits);
+}
 
 struct GemmArgs {
     const uint16_t* scales;
     const uint8_t* zeros;
     float* y;
     float* partials;  // [2 * P][kMaxCols][kBN]
-    int* counters;    // [T]
+    int* counters;    // [T][kCountersPerTile]
     int* err;         // kernel error word
     int M, N, K, ng;
     int T, I;         // tiles, k-stages per tile
@@ -43,16 +46,10 @@ inline long long unit_begin(long long U, int P, int b) { return U * b / P; }
 // Grid size from (N, K, bits) and the SM count only (never from M).
 int choose_grid(int T, int I, int sm_count);
 
-// Per-bit-width launchers (one translation unit each).
-cudaError_t launch_gemm_b4(int group, int nt, const CUtensorMap& tmW, const CUtensorMap& tmX,
-                           const GemmArgs& a, cudaStream_t s);
-cudaError_t launch_gemm_b2(int group, int nt, const CUtensorMap& tmW, const CUtensorMap& tmX,
-                           const GemmArgs& a, cudaStream_t s);
-cudaError_t launch_gemm_b3(int group, int nt, const CUtensorMap& tmW, const CUtensorMap& tmX,
-                           const GemmArgs& a, cudaStream_t s);
-
-// Tensor-core (tcgen05) kernels, 4-bit and 2-bit codes.
+// Tensor-core (tcgen05) GEMM kernels, one translation unit per bit width.
 cudaError_t launch_gemm_tc_b4(int group, const CUtensorMap& tmW, const CUtensorMap& tmX,
+                              const GemmArgs& a, cudaStream_t s);
+cudaError_t launch_gemm_tc_b3(int group, const CUtensorMap& tmW, const CUtensorMap& tmX,
                               const GemmArgs& a, cudaStream_t s);
 cudaError_t launch_gemm_tc_b2(int group, const CUtensorMap& tmW, const CUtensorMap& tmX,
                               const GemmArgs& a, cudaStream_t s);
