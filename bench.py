@@ -180,10 +180,15 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------- our path
+# Sources of the dominant GEMM kernel: a recorded DRAM-traffic figure is used
+# only while these files are unchanged.
+GEMM_SOURCES = ("wq_gemm_tc.cuh", "wq_gemm_tc_b4.cu", "wq_ptx.cuh", "wq_internal.h")
+
+
 def kernel_source_digest() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "weight_only_bit_wq_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in GEMM_SOURCES:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
@@ -479,8 +484,7 @@ def main_ours(args):
 
     dom_ms, dom_b, dom_n = run_dominant(stack, args.m, stream, args.steps, args.warmup, dist)
     dom_ms = reduce_max(dist, dom_ms, device)
-    nt = 1 if args.m <= 8 else 2
-    kernel_key = f"gemm_kernel<4,128,{nt}> N=34816 K=5120 M={args.m}"
+    kernel_key = f"gemm_tc_kernel<4,128> N=34816 K=5120 M={args.m}"
     achieved = dom_b["total"] / (dom_ms * 1e-3) / 1e9
 
     configs = None
