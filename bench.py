@@ -119,6 +119,13 @@ def reduce_sum(dist, value: float, device=None) -> float:
     return float(t.item())
 
 
+def whole_job_gbs(dist, bytes_this_rank: float, ms_this_rank: float, device=None):
+    """(GB/s, slowest rank's ms, bytes of all ranks): every rank's bytes over the max time."""
+    ms_max = reduce_max(dist, ms_this_rank, device)
+    total = reduce_sum(dist, float(bytes_this_rank), device)
+    return total / (ms_max * 1e-3) / 1e9, ms_max, total
+
+
 # ----------------------------------------------------------------- clocks
 class ClockSampler:
     """nvidia-smi clock / throttle samples every 200 ms while active."""
@@ -466,10 +473,8 @@ def main_ours(args):
     head = run_sweep_point(stack, args.m, stream, args.steps, args.warmup, dist, clocks=clocks,
                            e2e=True)
     sb = stack.step_bytes(args.m)
-    ms_max = reduce_max(dist, head["ms_per_step"], device)
-    packed_all = reduce_sum(dist, float(sb["packed"]), device)
+    value, ms_max, packed_all = whole_job_gbs(dist, sb["packed"], head["ms_per_step"], device)
     e2e_max = reduce_max(dist, head["e2e_ms"], device)
-    value = packed_all / (ms_max * 1e-3) / 1e9
 
     sweep = []
     if not args.no_sweep:
