@@ -256,6 +256,14 @@ class StepStack:
         # activations for up to 16 rows per projection (row m never depends on M)
         self.x16 = [synth.gen_x(p) for p in self.projs]
         self.ws = wq.new_workspace(16, 34816, 17408, 128, 4, device=device)
+        self.after = layer_dependencies(len(self.projs))
+        self.ws_fused = None  # sized from the first fused descriptor set (independent of M)
+
+    def fused_workspace(self, cdescs):
+        if self.ws_fused is None:
+            self.ws_fused = self.wq.new_step_workspace(cdescs, self.wq.WQ_STEP_FUSED,
+                                                       device=self.device)
+        return self.ws_fused
 
     def buffers(self, M):
         """Contiguous device X/Y for all projections at row count M, plus descriptors."""
@@ -268,11 +276,11 @@ class StepStack:
         ny = sum(M * p.N for p in self.projs)
         y_dev = torch.empty(ny, dtype=torch.float32, device=self.device)
         descs, xo, yo = [], 0, 0
-        for p, (wqw, s, z) in zip(self.projs, self.weights):
+        for i, (p, (wqw, s, z)) in enumerate(zip(self.projs, self.weights)):
             nx = M * p.K
             descs.append(dict(x=x_dev[xo:xo + nx], wq=wqw, scales=s, zeros=z,
                               y=y_dev[yo:yo + M * p.N], M=M, N=p.N, K=p.K, group=p.group,
-                              bits=p.bits))
+                              bits=p.bits, after=self.after[i]))
             xo += nx
             yo += M * p.N
         return x_host, x_dev, y_dev, descs
@@ -285,20 +293,52 @@ class StepStack:
         return tot
 
 
-def run_sweep_point(stack, M, stream, steps, warmup, dist, clocks=None, e2e=False):
+def layer_dependencies(n):
+    """`after` of each projection of the step (6 per layer: q, k, v, o, gate/up, down): q, k
+    and v read the layer input (the previous layer's down output), o reads attention over q, k,
+    v, gate/up reads o (through the residual and norm), down reads gate/up (through the
+    activation).  Only the ordering is modelled: the synthetic X buffers are not computed."""
+    after = []
+    for i in range(n):
+        base, j = i - i % 6, i % 6
+        after.append(base - 1 if j < 3 else base + j - 1)
+    return after
+
+
+def count_runs(descs):
+    """Fused launches per step: runs of consecutive projections of one format."""
+    runs, prev = 0, None
+    for d in descs:
+        key = (d["bits"], d["group"])
+        runs += key != prev
+        prev = key
+    return runs
+
+
+def run_sweep_point(stack, M, stream, steps, warmup, dist, clocks=None, e2e=False, mode="fused"):
+    """ms per step of the whole stack, as one CUDA graph: fused (one persistent launch per
+    step, honouring the layer dependency chain), fused-independent (no dependencies) or
+    sequential (one launch per projection)."""
     import torch
 
     wq = stack.wq
     x_host, x_dev, y_dev, descs = stack.buffers(M)
+    if mode == "fused-independent":
+        for d in descs:
+            d["after"] = -1
     cd = wq.make_descs(descs)
     stream.wait_stream(torch.cuda.current_stream())
-    graph = wq.StepGraph(cd, stack.ws, stream=stream)
+    if mode == "sequential":
+        ws, flags, launches = stack.ws, 0, len(descs)
+    else:
+        ws, flags, launches = stack.fused_workspace(cd), wq.WQ_STEP_FUSED, count_runs(descs)
+    graph = wq.StepGraph(cd, ws, stream=stream, flags=flags)
     if clocks is not None:
         with clocks:
             ms = time_launches(lambda: graph.launch(stream=stream), stream, steps, warmup, dist)
     else:
         ms = time_launches(lambda: graph.launch(stream=stream), stream, steps, warmup, dist)
-    out = {"M": M, "ms_per_step": ms, "launches_per_step": len(descs)}
+    out = {"M": M, "ms_per_step": ms, "launches_per_step": launches, "projections": len(descs)}
     if e2e:
         y_host = torch.empty(y_dev.numel(), dtype=torch.float32).pin_memory()
 
@@ -312,7 +352,7 @@ def run_sweep_point(stack, M, stream, steps, warmup, dist, clocks=None, e2e=Fals
         out["e2e_ms"] = ms_e2e
         out["h2d_bytes"] = x_host.numel() * 2
         out["d2h_bytes"] = y_host.numel() * 4
-    wq.wq_check_workspace(stack.ws, stream=stream)
+    wq.wq_check_workspace(ws, stream=stream)
     graph.close()
     return out
 
@@ -323,7 +363,7 @@ def run_dominant(stack, M, stream, steps, warmup, dist):
 
     wq = stack.wq
     _, _, _, descs = stack.buffers(M)
-    sel = [d for d, p in zip(descs, stack.projs) if p.name.endswith("gate_up")]
+    sel = [dict(d, after=-1) for d, p in zip(descs, stack.projs) if p.name.endswith("gate_up")]
     graph = wq.StepGraph(wq.make_descs(sel), stack.ws, stream=stream)
     stream.wait_stream(torch.cuda.current_stream())
     ms = time_launches(lambda: graph.launch(stream=stream), stream, max(3, steps // 2), 2, dist)
@@ -436,7 +476,10 @@ DATA = ("synthetic, seeded SplitMix64: codes U{0..15}, bf16 scales U(0.005,0.02)
 
 
 def _config(M, layers, world):
-    return {"workload": WORKLOAD, "M": M, "layers": layers, "launches_per_step": 6 * layers,
+    return {"workload": WORKLOAD, "M": M, "layers": layers, "launches_per_step": 1,
+            "mode": "one persistent launch per step (WQ_STEP_FUSED) honouring the layer "
+                    "dependency chain: q, k, v after the previous down; o after q, k, v; "
+                    "gate/up after o; down after gate/up",
             "l2": "inputs larger than L2 (every step streams all packed weights; no flush)",
             "parallelism": f"{world} independent replicas" if world > 1 else "one GPU"}
 
@@ -483,14 +526,28 @@ def main_ours(args):
             b = stack.step_bytes(M)
             ms = reduce_max(dist, r["ms_per_step"], device)
             sweep.append({"M": M, "ms_per_step": round(ms, 4),
-                          "us_per_call": round(ms * 1e3 / r["launches_per_step"], 3),
+                          "us_per_projection": round(ms * 1e3 / r["projections"], 3),
                           "weight_gbs": round(b["packed"] / (ms * 1e-3) / 1e9, 1),
                           "roofline_frac": round(b["total"] / (ms * 1e-3) / 1e9 / peak, 4)})
+    # the same step without dependencies, and as one launch per projection
+    modes = {}
+    for mode in ("fused-independent", "sequential"):
+        r = run_sweep_point(stack, args.m, stream, max(3, args.steps // 4), 2, dist, mode=mode)
+        ms = reduce_max(dist, r["ms_per_step"], device)
+        modes[mode] = {"ms_per_step": round(ms, 4), "launches_per_step": r["launches_per_step"],
+                       "weight_gbs": round(sb["packed"] / (ms * 1e-3) / 1e9, 1)}
 
+    # dominant kernel: the fused step kernel, one launch per step
+    kernel_key = f"gemm_tc_kernel<4,128,fused> step 64 layers M={args.m}"
+    achieved = sb["total"] / (ms_max * 1e-3) / 1e9
+    # the largest projection alone, one launch per call (context for the fused figure)
     dom_ms, dom_b, dom_n = run_dominant(stack, args.m, stream, args.steps, args.warmup, dist)
     dom_ms = reduce_max(dist, dom_ms, device)
-    kernel_key = f"gemm_tc_kernel<4,128> N=34816 K=5120 M={args.m}"
-    achieved = dom_b["total"] / (dom_ms * 1e-3) / 1e9
+    single = {"kernel": f"gemm_tc_kernel<4,128> N=34816 K=5120 M={args.m}",
+              "launch_us": round(dom_ms * 1e3, 3), "bytes_per_launch": dom_b["total"],
+              "achieved_gbs": round(dom_b["total"] / (dom_ms * 1e-3) / 1e9, 1),
+              "frac": round(dom_b["total"] / (dom_ms * 1e-3) / 1e9 / peak, 4),
+              "timing": f"CUDA events around a graph of {dom_n} launches (one per layer)"}
 
     configs = None
     if rank == 0 and not args.no_configs:
@@ -505,16 +562,17 @@ def main_ours(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": DATA, "config": _config(args.m, args.layers, world),
-            "us_per_call": round(ms_max * 1e3 / head["launches_per_step"], 3),
+            "us_per_projection": round(ms_max * 1e3 / head["projections"], 3),
             "step_bytes": sb["total"], "step_packed_bytes": sb["packed"],
             "roofline_frac_step": round(sb["total"] / (ms_max * 1e-3) / 1e9 / peak, 4),
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                          "unit": "GB/s", "frac": round(achieved / peak, 4),
                          "traffic": recorded_traffic(kernel_key), "kernel": kernel_key,
-                         "bytes_per_launch": dom_b["total"],
-                         "launch_us": round(dom_ms * 1e3, 3),
-                         "timing": f"CUDA events around a graph of {dom_n} launches (one per layer)",
+                         "bytes_per_launch": sb["total"],
+                         "launch_us": round(ms_max * 1e3, 3),
+                         "timing": "CUDA events around the step graph (one fused launch per step)",
                          "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)"},
+            "step_modes": modes, "single_launch": single,
             "cpu_baseline": cpu,
             "e2e": {"value": round(packed_all / (e2e_max * 1e-3) / 1e9, 1), "unit": "GB/s",
                     "h2d_bytes_per_step": head["h2d_bytes"], "d2h_bytes_per_step": head["d2h_bytes"],
@@ -567,7 +625,8 @@ def main_reference(args):
 
 
 def main_profile(args):
-    """A few plain calls of one seeded config on cuda:0 (small enough for ncu)."""
+    """A few plain calls of one seeded config on cuda:0 (small enough for ncu); config "step"
+    runs the fused decode step of --layers layers instead."""
     import numpy as np
     import torch
 
@@ -577,6 +636,19 @@ def main_profile(args):
 
     __graft_entry__.build()
     device = torch.device("cuda", 0)
+    if args.profile_config == "step":
+        stack = StepStack(args.layers, device)
+        _, _, _, descs = stack.buffers(args.m)
+        cd = wq.make_descs(descs)
+        ws = stack.fused_workspace(cd)
+        for _ in range(args.calls):
+            wq.wq_step_run(cd, ws, flags=wq.WQ_STEP_FUSED)
+        torch.cuda.synchronize()
+        wq.wq_check_workspace(ws)
+        b = stack.step_bytes(args.m)
+        print(json.dumps({"profile_config": "step", "layers": args.layers, "M": args.m,
+                          "calls": args.calls, "bytes_per_call": b["total"]}))
+        return 0
     p = synth.CONFIGS[args.profile_config]
     if args.m != HEADLINE_M:
         p = p.with_m(args.m) if p.x_row_seeds is None or args.m <= len(p.x_row_seeds) else p

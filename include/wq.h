@@ -160,9 +160,10 @@ wq_status_t wq_gemm_noalloc(const uint16_t* x, const uint32_t* wq, const uint16_
 wq_status_t wq_check_workspace(void* workspace, void* stream);
 
 /* ---------------------------------------------------------------------------
- * Decode-step driver: a whole layer stack's projections back to back on one
- * stream (OpenJet news page, paragraph "并行解码的原理": every projection of
- * every layer streams its weights once per step).
+ * Decode-step driver: a whole layer stack's projections on one stream
+ * (OpenJet news page, paragraph "并行解码的原理": every projection of every
+ * layer streams its weights once per step, and the whole step runs as one
+ * persistent kernel with no per-layer launch).
  * ------------------------------------------------------------------------ */
 typedef struct wq_proj_desc {
     const uint16_t* x;       /* [M][K] bf16 */
@@ -171,19 +172,53 @@ typedef struct wq_proj_desc {
     const uint8_t* zeros;    /* [N][K/G] */
     float* y;                /* [M][N] fp32 */
     int M, N, K, group, bits;
+    /* Fused mode only: x is produced by projections 0..after of the same
+     * call (through whatever the caller computes in between), so it is read
+     * only once those have written all of y; -1 = x is ready when the call
+     * starts.  Must be smaller than the projection's own index.  Ignored in
+     * sequential mode, where stream order already serialises everything. */
+    int after;
 } wq_proj_desc_t;
 
-/* Run `count` projections in order on `stream` (one wq_gemm each). */
+/* Step modes.
+ * 0 (sequential): one wq_gemm launch per projection, in order.
+ * WQ_STEP_FUSED: one persistent launch per run of consecutive projections
+ *   with the same bit width and group size.  The launch streams the units of
+ *   all its projections back to back (stream-K across projection
+ *   boundaries), so projections overlap unless `after` says otherwise;
+ *   packed weights of a waiting projection are still streamed in while it
+ *   waits, only its X is held back.  Launches that wait are cooperative
+ *   (all CTAs resident).  The split-K order differs from single calls, so
+ *   results agree with wq_gemm to rounding, not bit for bit; a row alone is
+ *   still bit-identical to the same row stacked. */
+#define WQ_STEP_FUSED 1u
+
+/* Workspace bytes for a step in the given mode (0 for invalid input).  In
+ * fused mode it holds the error word, split-K partials and counters, the
+ * per-projection completion counters and the projection table. */
+size_t wq_step_workspace_bytes(const wq_proj_desc_t* projs, int count, unsigned flags);
+
+/* Run the step once.  Sequential mode accepts any workspace wq_gemm accepts
+ * (NULL = the library buffer); fused mode needs `workspace` of at least
+ * wq_step_workspace_bytes(), 16-byte aligned, zeroed once (wq_workspace_init)
+ * before its first use. */
 wq_status_t wq_step_run(const wq_proj_desc_t* projs, int count, void* workspace,
                         size_t workspace_bytes, void* stream);
+wq_status_t wq_step_run_ex(const wq_proj_desc_t* projs, int count, unsigned flags,
+                           void* workspace, size_t workspace_bytes, void* stream);
 
 typedef struct wq_step_graph* wq_step_graph_t;
 
-/* Capture the same launch sequence once into a CUDA graph (no host work per
- * replay).  The descriptors' pointers are baked in: the buffers must stay
- * alive and in place while the graph exists.  `workspace` must be non-NULL. */
+/* Capture the step once into a CUDA graph (no host work per replay).  The
+ * descriptors' pointers are baked in: the buffers must stay alive and in
+ * place while the graph exists.  `workspace` must be non-NULL.  In fused mode
+ * the graph owns a device copy of the projection table (allocated here, freed
+ * by wq_step_graph_destroy). */
 wq_status_t wq_step_graph_create(const wq_proj_desc_t* projs, int count, void* workspace,
                                  size_t workspace_bytes, void* stream, wq_step_graph_t* out);
+wq_status_t wq_step_graph_create_ex(const wq_proj_desc_t* projs, int count, unsigned flags,
+                                    void* workspace, size_t workspace_bytes, void* stream,
+                                    wq_step_graph_t* out);
 wq_status_t wq_step_graph_launch(wq_step_graph_t graph, void* stream);
 void wq_step_graph_destroy(wq_step_graph_t graph);
 

@@ -57,3 +57,125 @@ def test_step_run_and_graph_match_single_calls(M):
     err = rel_err(d["y"].cpu().numpy(), oracle_gemm(p, w, x))
     assert err <= REL_TOL and err <= ARITH_TOL
     wq.wq_check_workspace(ws)
+
+
+def _descs(wq, projs, after=None):
+    return wq.make_descs([dict(x=d["x"], wq=d["wq"], scales=d["s"], zeros=d["z"], y=d["y"], M=p.M,
+                               N=p.N, K=p.K, group=p.group, bits=p.bits,
+                               after=-1 if after is None else after[i])
+                          for i, (p, w, x, d) in enumerate(projs)])
+
+
+def _layer_after(n):
+    # the dependency chain of a decode layer, repeated: q, k, v read the layer
+    # input (the previous down), o waits for q, k, v, gate/up for o, down for gate/up
+    after = []
+    for i in range(n):
+        j = i % 6
+        base = i - j
+        after.append({0: base - 1, 1: base - 1, 2: base - 1, 3: base + 2, 4: base + 3,
+                      5: base + 4}[j] if i >= 1 else -1)
+    return [a if a < i else -1 for i, a in enumerate(after)]
+
+
+def _uniform_stack(M, bits, G, layers=2):
+    # a miniature decode layer (q, k, v, o, gate/up, down) in one format, so a
+    # fused launch holds whole layers and their dependency chain
+    shapes = [(640, 640), (640, 128), (640, 128), (640, 640), (640, 1792), (896, 640)]
+    projs = []
+    for i, (K, N) in enumerate(shapes * layers):
+        p = synth.Projection(f"u{i}", M, N, K, bits, G, 400, index=i)
+        w, x, d = to_dev_host_inputs(p)
+        d["y"] = torch.empty((M, N), dtype=torch.float32, device=dev())
+        projs.append((p, w, x, d))
+    return projs
+
+
+FUSED_FORMATS = [(4, 128), (3, 128), (2, 64), (4, 32), (3, 64), (2, 128)]
+
+
+@pytest.mark.parametrize("fmt", FUSED_FORMATS, ids=lambda f: f"b{f[0]}g{f[1]}")
+@pytest.mark.parametrize("deps", [False, True], ids=["independent", "layer-chain"])
+def test_fused_uniform_stack_matches_oracle(fmt, deps):
+    import weight_only_bit_wq_gb300 as wq
+    projs = _uniform_stack(7, *fmt)
+    after = _layer_after(len(projs)) if deps else None
+    descs = _descs(wq, projs, after)
+    ws = wq.new_step_workspace(descs, wq.WQ_STEP_FUSED)
+    for _ in range(2):  # the second run checks that counters were left clean
+        for p, w, x, d in projs:
+            d["y"].fill_(float("nan"))
+        wq.wq_step_run(descs, ws, flags=wq.WQ_STEP_FUSED)
+        torch.cuda.synchronize()
+        wq.wq_check_workspace(ws)
+        for p, w, x, d in projs:
+            err = rel_err(d["y"].cpu().numpy(), oracle_gemm(p, w, x))
+            assert err <= REL_TOL and err <= ARITH_TOL, (p.name, err)
+
+
+@pytest.mark.parametrize("deps", [False, True], ids=["independent", "layer-chain"])
+@pytest.mark.parametrize("M", [1, 12])
+def test_fused_step_matches_oracle(M, deps):
+    import weight_only_bit_wq_gb300 as wq
+    projs = _stack(M)
+    after = _layer_after(len(projs)) if deps else None
+    descs = _descs(wq, projs, after)
+    ws = wq.new_step_workspace(descs, wq.WQ_STEP_FUSED)
+    for _ in range(2):  # the second run checks that counters were left clean
+        for p, w, x, d in projs:
+            d["y"].fill_(float("nan"))
+        wq.wq_step_run(descs, ws, flags=wq.WQ_STEP_FUSED)
+        torch.cuda.synchronize()
+        wq.wq_check_workspace(ws)
+        for p, w, x, d in projs:
+            err = rel_err(d["y"].cpu().numpy(), oracle_gemm(p, w, x))
+            assert err <= REL_TOL and err <= ARITH_TOL, (p.name, err)
+
+
+def test_fused_graph_replays_bitwise_and_rows_are_batch_invariant():
+    import weight_only_bit_wq_gb300 as wq
+    M = 4
+    projs = _uniform_stack(M, 4, 128)
+    after = _layer_after(len(projs))
+    descs = _descs(wq, projs, after)
+    ws = wq.new_step_workspace(descs, wq.WQ_STEP_FUSED)
+    wq.wq_step_run(descs, ws, flags=wq.WQ_STEP_FUSED)
+    torch.cuda.synchronize()
+    ref = [d["y"].cpu().numpy().copy() for p, w, x, d in projs]
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    g = wq.StepGraph(descs, ws, stream=stream, flags=wq.WQ_STEP_FUSED)
+    for _ in range(3):
+        for p, w, x, d in projs:
+            d["y"].fill_(float("nan"))
+        g.launch(stream=stream)
+        stream.synchronize()
+        for (p, w, x, d), r in zip(projs, ref):
+            assert (d["y"].cpu().numpy().view(np.uint32) == r.view(np.uint32)).all(), p.name
+    g.close()
+    wq.wq_check_workspace(ws)
+    # each row alone (M = 1, same projections otherwise) equals its row of the stack
+    for row in (0, 3):
+        alone = []
+        for p, w, x, d in projs:
+            xr = d["x"][row:row + 1].contiguous()
+            alone.append(dict(x=xr, wq=d["wq"], scales=d["s"], zeros=d["z"],
+                              y=torch.empty((1, p.N), dtype=torch.float32, device=dev()),
+                              M=1, N=p.N, K=p.K, group=p.group, bits=p.bits))
+        for i, a in enumerate(alone):
+            a["after"] = after[i]
+        d1 = wq.make_descs(alone)
+        ws1 = wq.new_step_workspace(d1, wq.WQ_STEP_FUSED)
+        wq.wq_step_run(d1, ws1, flags=wq.WQ_STEP_FUSED)
+        torch.cuda.synchronize()
+        for a, r in zip(alone, ref):
+            assert (a["y"].cpu().numpy()[0].view(np.uint32) == r[row].view(np.uint32)).all()
+
+
+def test_fused_step_bad_dependency_rejected():
+    import weight_only_bit_wq_gb300 as wq
+    projs = _stack(1)[:3]
+    descs = _descs(wq, projs, [-1, 1, 0])  # projection 1 cannot wait for itself
+    assert wq.wq_step_workspace_bytes(descs, wq.WQ_STEP_FUSED) == 0
+    with pytest.raises(wq.WQError):
+        wq.wq_step_run(descs, wq.new_workspace(1, 640, 640, 128, 4), flags=wq.WQ_STEP_FUSED)

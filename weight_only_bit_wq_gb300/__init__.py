@@ -24,8 +24,12 @@ WQ_OK, WQ_ERR_INVALID_ARG, WQ_ERR_UNSUPPORTED, WQ_ERR_CUDA, WQ_ERR_TIMEOUT = ran
 
 EXPORTED = ("wq_abi_version", "wq_status_string", "wq_last_cuda_error", "wq_packed_words_per_row",
             "wq_pack", "wq_unpack", "wq_dequant", "wq_workspace_bytes", "wq_workspace_init",
-            "wq_gemm", "wq_check_workspace", "wq_step_run", "wq_step_graph_create",
+            "wq_gemm", "wq_check_workspace", "wq_step_workspace_bytes", "wq_step_run",
+            "wq_step_run_ex", "wq_step_graph_create", "wq_step_graph_create_ex",
             "wq_step_graph_launch", "wq_step_graph_destroy")
+
+# Step modes (include/wq.h).
+WQ_STEP_FUSED = 1
 
 
 class WQError(RuntimeError):
@@ -42,7 +46,7 @@ class ProjDesc(ctypes.Structure):
     _fields_ = [("x", ctypes.c_void_p), ("wq", ctypes.c_void_p), ("scales", ctypes.c_void_p),
                 ("zeros", ctypes.c_void_p), ("y", ctypes.c_void_p), ("M", ctypes.c_int),
                 ("N", ctypes.c_int), ("K", ctypes.c_int), ("group", ctypes.c_int),
-                ("bits", ctypes.c_int)]
+                ("bits", ctypes.c_int), ("after", ctypes.c_int)]
 
 
 _LIB: Optional[ctypes.CDLL] = None
@@ -67,14 +71,19 @@ def _lib() -> ctypes.CDLL:
             "wq_workspace_init": ([P, S, P], I),
             "wq_gemm": ([P, P, P, P, P, I, I, I, I, I, P, S, P], I),
             "wq_check_workspace": ([P, P], I),
+            "wq_step_workspace_bytes": ([P, I, ctypes.c_uint], S),
             "wq_step_run": ([P, I, P, S, P], I),
+            "wq_step_run_ex": ([P, I, ctypes.c_uint, P, S, P], I),
             "wq_step_graph_create": ([P, I, P, S, P, P], I),
+            "wq_step_graph_create_ex": ([P, I, ctypes.c_uint, P, S, P, P], I),
             "wq_step_graph_launch": ([P, P], I),
             "wq_step_graph_destroy": ([P], None),
             "wq_internal_schedule_check": ([ctypes.c_longlong, I], I),
         }
         for name, (args, res) in sig.items():
-            fn = getattr(lib, name)
+            fn = getattr(lib, name, None)
+            if fn is None:  # an older library: the call fails when it is made
+                continue
             fn.argtypes = args
             fn.restype = res
         _LIB = lib
@@ -170,30 +179,47 @@ def wq_check_workspace(workspace=None, stream=None) -> None:
 
 
 def make_descs(projs: Sequence[dict]) -> ctypes.Array:
-    """Descriptor array from dicts with keys x, wq, scales, zeros, y, M, N, K, group, bits."""
+    """Descriptor array from dicts with keys x, wq, scales, zeros, y, M, N, K, group, bits and
+    optionally after (fused mode: x depends on projections 0..after; default -1)."""
     arr = (ProjDesc * len(projs))()
     for i, p in enumerate(projs):
         arr[i] = ProjDesc(p["x"].data_ptr(), p["wq"].data_ptr(), p["scales"].data_ptr(),
                           p["zeros"].data_ptr(), p["y"].data_ptr(), p["M"], p["N"], p["K"],
-                          p["group"], p["bits"])
+                          p["group"], p["bits"], p.get("after", -1))
     return arr
 
 
-def wq_step_run(descs: ctypes.Array, workspace: torch.Tensor, stream=None) -> None:
-    _check(_lib().wq_step_run(ctypes.cast(descs, ctypes.c_void_p), len(descs), _ptr(workspace),
-                              workspace.numel(), _stream(stream)), "wq_step_run")
+def wq_step_workspace_bytes(descs: ctypes.Array, flags: int = 0) -> int:
+    return int(_lib().wq_step_workspace_bytes(ctypes.cast(descs, ctypes.c_void_p), len(descs),
+                                              flags))
+
+
+def new_step_workspace(descs: ctypes.Array, flags: int = 0, device=None) -> torch.Tensor:
+    """A zeroed workspace for a step of these descriptors in this mode."""
+    n = wq_step_workspace_bytes(descs, flags)
+    if n == 0:
+        raise ValueError("invalid step descriptors")
+    ws = torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
+    return ws
+
+
+def wq_step_run(descs: ctypes.Array, workspace: torch.Tensor, stream=None, flags: int = 0) -> None:
+    _check(_lib().wq_step_run_ex(ctypes.cast(descs, ctypes.c_void_p), len(descs), flags,
+                                 _ptr(workspace), workspace.numel(), _stream(stream)),
+           "wq_step_run_ex")
 
 
 class StepGraph:
     """A captured decode step (wq_step_graph_create / _launch / _destroy)."""
 
-    def __init__(self, descs: ctypes.Array, workspace: torch.Tensor, stream=None):
+    def __init__(self, descs: ctypes.Array, workspace: torch.Tensor, stream=None, flags: int = 0):
         self._descs = descs
         self._ws = workspace
         h = ctypes.c_void_p(0)
-        _check(_lib().wq_step_graph_create(ctypes.cast(descs, ctypes.c_void_p), len(descs),
-                                           _ptr(workspace), workspace.numel(), _stream(stream),
-                                           ctypes.byref(h)), "wq_step_graph_create")
+        _check(_lib().wq_step_graph_create_ex(ctypes.cast(descs, ctypes.c_void_p), len(descs),
+                                              flags, _ptr(workspace), workspace.numel(),
+                                              _stream(stream), ctypes.byref(h)),
+               "wq_step_graph_create_ex")
         self._h = h
 
     def launch(self, stream=None) -> None:

@@ -103,7 +103,7 @@ int choose_grid(int T, int I, int sm_count) {
 
 extern "C" {
 
-int wq_abi_version(void) { return 100; }
+int wq_abi_version(void) { return 101; }
 
 const char* wq_status_string(wq_status_t s) {
     switch (s) {
@@ -254,27 +254,65 @@ wq_status_t library_workspace(DeviceInfo* d, size_t need, void** out) {
 
 }  // namespace
 
+namespace wq {
+
+wq_status_t host_cuda_fail(cudaError_t e) { return cuda_fail(e); }
+
+wq_status_t host_sm_count(int* sms) {
+    DeviceInfo* d;
+    if (wq_status_t st = device_info(&d)) return st;
+    *sms = d->sm_count;
+    return WQ_OK;
+}
+
+wq_status_t host_check_gemm(const uint16_t* x, const uint32_t* wq, const uint16_t* scales,
+                            const uint8_t* zeros, const float* y, int M, int N, int K, int group,
+                            int bits) {
+    if (!valid_bits(bits) || !valid_group(group) || M < 0 || M > kMaxCols || N < 0 || K < 0 ||
+        K % group != 0)
+        return WQ_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return WQ_OK;
+    if (!y || !aligned(y, 4)) return WQ_ERR_INVALID_ARG;
+    if (K == 0) return WQ_OK;
+    if (!x || !wq || !scales || !zeros || !aligned(x, 16) || !aligned(wq, 16) || !aligned(scales, 2))
+        return WQ_ERR_INVALID_ARG;
+    return WQ_OK;
+}
+
+wq_status_t host_encode_proj(const uint16_t* x, const uint32_t* wq, const uint16_t* scales,
+                             const uint8_t* zeros, int M, int N, int K, int group, int bits,
+                             CUtensorMap* tmW, CUtensorMap* tmX, int* x3d, int* meta_vec) {
+    const int W = static_cast<int>(wq_packed_words_per_row(K, bits));
+    const int sv = tc_stage_values(bits, group);
+    if (wq_status_t st = encode_maps(x, wq, M, N, K, W, tmW, tmX)) return st;
+    *x3d = K % 64 == 0 ? 1 : 0;
+    if (*x3d)
+        if (wq_status_t st = encode_x3d(x, M, K, sv / 64, tmX)) return st;
+    const int ng = K / group;
+    const int gps = sv / group;
+    const bool gps_pow2 = (gps & (gps - 1)) == 0;
+    *meta_vec = (gps_pow2 && ng % gps == 0 && aligned(scales, 16) && aligned(zeros, 16)) ? 1 : 0;
+    return WQ_OK;
+}
+
+}  // namespace wq
+
 extern "C" {
 
 wq_status_t wq_gemm(const uint16_t* x, const uint32_t* wq, const uint16_t* scales,
                     const uint8_t* zeros, float* y, int M, int N, int K, int group, int bits,
                     void* workspace, size_t workspace_bytes, void* stream) {
-    if (!valid_bits(bits) || !valid_group(group) || M < 0 || M > wq::kMaxCols || N < 0 || K < 0 ||
-        K % group != 0)
-        return WQ_ERR_INVALID_ARG;
+    if (wq_status_t st = wq::host_check_gemm(x, wq, scales, zeros, y, M, N, K, group, bits))
+        return st;
     if (M == 0 || N == 0) return WQ_OK;
-    if (!y || !aligned(y, 4)) return WQ_ERR_INVALID_ARG;
     cudaStream_t s = as_stream(stream);
     if (K == 0) {  // empty sum
         cudaError_t e = cudaMemsetAsync(y, 0, static_cast<size_t>(M) * N * sizeof(float), s);
         return e == cudaSuccess ? WQ_OK : cuda_fail(e);
     }
-    if (!x || !wq || !scales || !zeros || !aligned(x, 16) || !aligned(wq, 16) || !aligned(scales, 2))
-        return WQ_ERR_INVALID_ARG;
     DeviceInfo* d;
     if (wq_status_t st = device_info(&d)) return st;
 
-    const int W = static_cast<int>(wq_packed_words_per_row(K, bits));
     const int T = (N + wq::kBN - 1) / wq::kBN;
     const int sv = wq::tc_stage_values(bits, group);
     const int I = (K + sv - 1) / sv;
@@ -287,12 +325,10 @@ wq_status_t wq_gemm(const uint16_t* x, const uint32_t* wq, const uint16_t* scale
     }
 
     CUtensorMap tmW, tmX;
-    if (wq_status_t st = encode_maps(x, wq, M, N, K, W, &tmW, &tmX)) return st;
-    const bool x3d = K % 64 == 0;
-    if (x3d)
-        if (wq_status_t st = encode_x3d(x, M, K, sv / 64, &tmX)) return st;
-
     wq::GemmArgs a;
+    if (wq_status_t st = wq::host_encode_proj(x, wq, scales, zeros, M, N, K, group, bits, &tmW,
+                                              &tmX, &a.x3d, &a.meta_vec))
+        return st;
     a.scales = scales;
     a.zeros = zeros;
     a.y = y;
@@ -308,10 +344,6 @@ wq_status_t wq_gemm(const uint16_t* x, const uint32_t* wq, const uint16_t* scale
     a.I = I;
     a.U = static_cast<long long>(T) * I;
     a.P = wq::choose_grid(T, I, d->sm_count);
-    const int gps = sv / group;
-    const bool gps_pow2 = (gps & (gps - 1)) == 0;
-    a.meta_vec = (gps_pow2 && a.ng % gps == 0 && aligned(scales, 16) && aligned(zeros, 16)) ? 1 : 0;
-    a.x3d = x3d ? 1 : 0;
 
     cudaError_t e;
     if (bits == 4)

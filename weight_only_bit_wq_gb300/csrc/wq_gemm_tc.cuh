@@ -151,7 +151,8 @@ struct RowMeta {
     uint32_t s[kS];
     uint32_t z[kZ];
 
-    __device__ __forceinline__ void load(const GemmArgs& a, int n, long long g0, bool vec) {
+    template <class V>
+    __device__ __forceinline__ void load(const V& a, int n, long long g0) {
 #pragma unroll
         for (int j = 0; j < kS; ++j) s[j] = 0;
 #pragma unroll
@@ -159,7 +160,7 @@ struct RowMeta {
         if (n >= a.N) return;
         const long long base = static_cast<long long>(n) * a.ng + g0;
         if constexpr (GPS == 4 || GPS == 8 || GPS == 16) {
-            if (vec) {
+            if (a.meta_vec) {
                 const uint16_t* sp = a.scales + base;
                 const uint8_t* zp = a.zeros + base;
                 if constexpr (GPS == 4) {
@@ -247,9 +248,9 @@ __device__ __forceinline__ void tmem_st_cols<32>(uint32_t taddr, const uint32_t 
         : "memory");
 }
 
-__device__ __forceinline__ void record_error_tc(const GemmArgs& a, volatile int* abort_flag) {
+__device__ __forceinline__ void record_error_tc(int* err, volatile int* abort_flag) {
     *abort_flag = 1;
-    atomicExch(a.err, 1);
+    atomicExch(err, 1);
 }
 
 // Warp-uniform bounded wait: true only if every lane saw the phase complete.
@@ -388,39 +389,188 @@ __device__ __forceinline__ void write_group_rt(uint32_t row_sw, uint32_t tA,
     }
 }
 
+// Projection data as the warps see it.
+struct ProjView {
+    const CUtensorMap* tmW;
+    const CUtensorMap* tmX;
+    const uint16_t* scales;
+    const uint8_t* zeros;
+    float* y;
+    long long uoff;  // first global unit
+    int M, N, ng, T, I, toff, after, phase;
+    bool meta_vec, x3d;
+};
+
+// Kernel-wide context: one projection from the launch parameters, or a table
+// of projections in device memory (fused step).
+struct Ctx {
+    const ProjDev* proj;    // nullptr: the single projection `one`, one phase
+    const PhaseDev* phase;
+    int nproj, nphase;
+    ProjView one;
+    float* partials;
+    int* counters;
+    int* done;
+    int* err;
+    long long U;
+    int P;
+
+    __device__ __forceinline__ ProjView view(int p) const {
+        if (proj == nullptr) return one;
+        const ProjDev& d = proj[p];
+        ProjView v;
+        v.tmW = &d.tmW;
+        v.tmX = &d.tmX;
+        v.scales = d.scales;
+        v.zeros = d.zeros;
+        v.y = d.y;
+        v.uoff = d.uoff;
+        v.M = d.M;
+        v.N = d.N;
+        v.ng = d.ng;
+        v.T = d.T;
+        v.I = d.I;
+        v.toff = d.toff;
+        v.after = d.after;
+        v.phase = d.phase;
+        v.meta_vec = d.meta_vec != 0;
+        v.x3d = d.x3d != 0;
+        return v;
+    }
+    // Projection holding global unit u (binary search over the unit offsets).
+    __device__ __forceinline__ int proj_of_unit(long long u) const {
+        if (proj == nullptr) return 0;
+        int lo = 0, hi = nproj - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (proj[mid].uoff <= u)
+                lo = mid;
+            else
+                hi = mid - 1;
+        }
+        return lo;
+    }
+    // Phase s covers global units [phase_uoff(s), phase_uoff(s) + phase_units(s)).
+    __device__ __forceinline__ long long phase_uoff(int s) const {
+        return phase == nullptr ? 0 : phase[s].uoff;
+    }
+    __device__ __forceinline__ long long phase_units(int s) const {
+        return phase == nullptr ? U : phase[s].U;
+    }
+    // CTAs sharing phase s: all of them, or one per unit when the phase is
+    // smaller than the grid (so that every share is contiguous and non-empty).
+    __device__ __forceinline__ int phase_ctas(int s) const {
+        const long long Us = phase_units(s);
+        return Us < P ? static_cast<int>(Us) : P;
+    }
+    // floor(n / d) for non-negative n and positive d; 32-bit when it fits
+    // (64-bit integer division is a long software sequence).
+    __device__ __forceinline__ static long long div_fast(unsigned long long n, unsigned long long d) {
+        if (n <= 0xffffffffull && d <= 0xffffffffull)
+            return static_cast<long long>(static_cast<uint32_t>(n) / static_cast<uint32_t>(d));
+        return static_cast<long long>(n / d);
+    }
+    // CTA b's share of phase s: [sub_lo(s, b), sub_lo(s, b + 1)); empty for b >= phase_ctas(s).
+    __device__ __forceinline__ long long sub_lo(int s, int b) const {
+        const int Ps = phase_ctas(s);
+        const unsigned long long Us = static_cast<unsigned long long>(phase_units(s));
+        return phase_uoff(s) + div_fast(Us * static_cast<unsigned>(b < Ps ? b : Ps),
+                                        static_cast<unsigned>(Ps));
+    }
+    // CTA whose share of phase s holds global unit u: ceil((x + 1) Ps / Us) - 1
+    // for the unit's index x within the phase.
+    __device__ __forceinline__ int owner(long long u, int s) const {
+        const unsigned long long Us = static_cast<unsigned long long>(phase_units(s));
+        const unsigned long long x = static_cast<unsigned long long>(u - phase_uoff(s));
+        return static_cast<int>(div_fast((x + 1) * static_cast<unsigned>(phase_ctas(s)) + Us - 1, Us)) - 1;
+    }
+};
+
+// A warp's position in its CTA's units: phase s, projection p, tile t,
+// k-stage i, global unit u (the CTA's share of phase s ends at u_end).
+struct Cursor {
+    int s, p, t, i;
+    long long u, u_end;
+    ProjView v;
+    // first non-empty share at or after phase s0
+    __device__ __forceinline__ void seek(const Ctx& c, int s0) {
+        for (s = s0; s < c.nphase; ++s) {
+            u = c.sub_lo(s, blockIdx.x);
+            u_end = c.sub_lo(s, blockIdx.x + 1);
+            if (u < u_end) break;
+        }
+        if (s >= c.nphase) return;
+        p = c.proj_of_unit(u);
+        v = c.view(p);
+        const long long l = u - v.uoff;
+        t = static_cast<int>(l / v.I);
+        i = static_cast<int>(l - static_cast<long long>(t) * v.I);
+    }
+    __device__ __forceinline__ void init(const Ctx& c) { seek(c, 0); }
+    __device__ __forceinline__ bool last_of_share() const { return u + 1 == u_end; }
+    __device__ __forceinline__ void next(const Ctx& c) {
+        if (++u == u_end) {
+            seek(c, s + 1);
+            return;
+        }
+        if (++i == v.I) {
+            i = 0;
+            if (++t == v.T) {
+                t = 0;
+                ++p;
+                v = c.view(p);
+            }
+        }
+    }
+};
+
 // End of a tile segment for one epilogue warp (rows 32 q + lane, all
 // accumulator columns): store Y, or publish the partial sums and let the
 // warp of the last CTA to finish the tile add all partials in k order.  Each
 // (tile, lane quarter) pair has its own arrival counter, so warps never wait
-// for one another.
-__device__ __forceinline__ void finish_rows(const GemmArgs& a, const float (&acc)[kN], int t,
-                                            bool whole, long long u_lo, int r, int q, int lane) {
+// for one another.  In a fused step the warp that writes the final Y rows
+// then counts them done for the projection.
+__device__ __forceinline__ void finish_rows(const Ctx& c, const ProjView& v, int p,
+                                            const float (&acc)[kN], int t, bool whole, int r,
+                                            int q, int lane) {
     const int n = t * kBN + r;
+    const int gt = v.toff + t;
+    auto count_done = [&]() {
+        if (c.proj != nullptr) {
+            __syncwarp();
+            if (lane == 0) red_add_release_gpu(c.done + p, 1);
+        }
+    };
     if (whole) {
-        if (n < a.N)
+        if (n < v.N)
 #pragma unroll
             for (int j = 0; j < kN; ++j)
-                if (j < a.M) a.y[static_cast<size_t>(j) * a.N + n] = acc[j];
+                if (j < v.M) v.y[static_cast<size_t>(j) * v.N + n] = acc[j];
+        count_done();
         return;
     }
-    const int t_first = static_cast<int>(u_lo / a.I);
-    float* mine = a.partials + static_cast<size_t>(2 * blockIdx.x + (t == t_first ? 0 : 1)) *
-                                   (kMaxCols * kBN);
+    // Slot 0 holds the partial of the tile a CTA's share of the phase starts in,
+    // slot 1 that of the tile it ends in (a share that started before this
+    // tile's first unit ends in it).
+    const long long tu0 = v.uoff + static_cast<long long>(t) * v.I;
+    const int own_role = c.sub_lo(v.phase, blockIdx.x) < tu0 ? 1 : 0;
+    float* mine = c.partials + static_cast<size_t>(2 * blockIdx.x + own_role) * (kMaxCols * kBN);
 #pragma unroll
     for (int j = 0; j < kN; ++j)
-        if (j < a.M) __stcg(mine + j * kBN + r, acc[j]);
+        if (j < v.M) __stcg(mine + j * kBN + r, acc[j]);
     // The warp barrier orders every lane's partial before lane 0's release
     // (acq_rel) increment; the reading warp's lane 0 acquires it and the next
     // warp barrier orders the other lanes' reads after that acquire.
     __syncwarp();
-    const long long tu0 = static_cast<long long>(t) * a.I;
-    const int b_first = static_cast<int>(((tu0 + 1) * a.P + a.U - 1) / a.U - 1);
-    const int b_last = static_cast<int>(((tu0 + a.I) * a.P + a.U - 1) / a.U - 1);
-    int* ctr = a.counters + static_cast<size_t>(t) * kCountersPerTile + q;
+    const int b_first = c.owner(tu0, v.phase);
+    const int b_last = c.owner(tu0 + v.I - 1, v.phase);
+    int* ctr = c.counters + static_cast<size_t>(gt) * kCountersPerTile + q;
     int last = 0;
     if (lane == 0) last = (atomic_add_acq_rel_gpu(ctr, 1) == b_last - b_first) ? 1 : 0;
     last = __shfl_sync(kFull, last, 0);
     if (!last) return;
+    // contributors after the first start their share inside this tile (slot 0)
+    const int first_role = c.sub_lo(v.phase, b_first) < tu0 ? 1 : 0;
     float tot[kN];
 #pragma unroll
     for (int j = 0; j < kN; ++j) tot[j] = 0.f;
@@ -429,19 +579,23 @@ __device__ __forceinline__ void finish_rows(const GemmArgs& a, const float (&acc
 #pragma unroll
             for (int j = 0; j < kN; ++j) tot[j] += acc[j];
         } else {
-            const int tb = static_cast<int>((a.U * b / a.P) / a.I);
-            const float* src =
-                a.partials + static_cast<size_t>(2 * b + (t == tb ? 0 : 1)) * (kMaxCols * kBN);
+            const float* src = c.partials +
+                               static_cast<size_t>(2 * b + (b == b_first ? first_role : 0)) *
+                                   (kMaxCols * kBN) +
+                               r;
+            float part[kN];
 #pragma unroll
-            for (int j = 0; j < kN; ++j)
-                if (j < a.M) tot[j] += __ldcg(src + j * kBN + r);
+            for (int j = 0; j < kN; ++j) part[j] = j < v.M ? __ldcg(src + j * kBN) : 0.f;
+#pragma unroll
+            for (int j = 0; j < kN; ++j) tot[j] += part[j];
         }
     }
-    if (n < a.N)
+    if (n < v.N)
 #pragma unroll
         for (int j = 0; j < kN; ++j)
-            if (j < a.M) a.y[static_cast<size_t>(j) * a.N + n] = tot[j];
+            if (j < v.M) v.y[static_cast<size_t>(j) * v.N + n] = tot[j];
     if (lane == 0) *ctr = 0;
+    count_done();
 }
 
 // Shared-memory barriers of one CTA.
@@ -456,6 +610,7 @@ struct Bars {
     uint64_t drain;      // every MMA complete
     uint32_t tmem_base;
     int abort_flag;
+    int n_units;         // units of this CTA (all its phase shares)
 };
 
 // Ring position: slot index and phase parity of a barrier ring of N entries.
@@ -473,9 +628,9 @@ struct Ring {
 // Unpack warp: turns the stage's packed words into A tiles, batch by batch.
 // HT is the warp's K part when fixed at compile time, -1 when read at run time.
 template <int BITS, int G, int HT, class B>
-__device__ __forceinline__ void unpack_warp(const GemmArgs& a, uint32_t smem_u32, B& bars,
+__device__ __forceinline__ void unpack_warp(const Ctx& c, uint32_t smem_u32, B& bars,
                                             uint32_t tmem, volatile int* abort_flag, int warp,
-                                            int lane, int n_units, int t_first, int i_first) {
+                                            int lane, int n_units) {
     using L = Lay<BITS, G>;
     using RM = RowMeta<L::kGPS>;
     const int h = HT >= 0 ? HT : (warp >> 2);
@@ -483,23 +638,20 @@ __device__ __forceinline__ void unpack_warp(const GemmArgs& a, uint32_t smem_u32
     const int r = 32 * q + lane;                                       // tile row == TMEM lane
     const uint32_t tl = tmem + (static_cast<uint32_t>(32 * q) << 16);  // lane quarter
     const uint32_t row_off = static_cast<uint32_t>(r * 128) | (static_cast<uint32_t>(lane & 7) << 4);
-    const bool vec = a.meta_vec != 0;
     bool dead = false;  // after a failed wait: no more shared or tensor memory work
 
     // Zero points are needed here only when they are subtracted on the CUDA
     // cores; otherwise the epilogue warps write the zero-point tiles.
-    int ft = t_first, fi = i_first;
+    Cursor fc;
+    if constexpr (!L::kZtc) fc.init(c);
     auto fetch = [&](RM& m) {
         if constexpr (!L::kZtc) {
-            m.load(a, ft * kBN + r, static_cast<long long>(fi) * L::kGPS, vec);
-            if (++fi == a.I) {
-                fi = 0;
-                ++ft;
-            }
+            m.load(fc.v, fc.t * kBN + r, static_cast<long long>(fc.i) * L::kGPS);
+            fc.next(c);
         }
     };
     auto fail = [&]() {
-        record_error_tc(a, abort_flag);
+        record_error_tc(c.err, abort_flag);
         dead = true;
     };
 
@@ -545,40 +697,37 @@ __device__ __forceinline__ void unpack_warp(const GemmArgs& a, uint32_t smem_u32
     }
 }
 
-// Epilogue warp (lane quarter q).  Per batch j of the CTA's schedule it
-// writes batch j's zero-point tiles (when the zero point is applied on the
-// tensor core), then reads batch j - 1's accumulators back, adds scale * D to
-// the row's 16 fp32 sums and ends tile segments.
+// Epilogue warp (lane quarter q).  Per unit it reads the unit's two batches
+// of accumulators back (adding scale * D to the row's 16 fp32 sums), writes
+// the next unit's zero-point tiles (when the zero point is applied on the
+// tensor core) in between, and ends tile segments.
 template <int BITS, int G, class B>
-__device__ __forceinline__ void epilogue_warp(const GemmArgs& a, B& bars, uint32_t tmem,
+__device__ __forceinline__ void epilogue_warp(const Ctx& c, B& bars, uint32_t tmem,
                                               volatile int* abort_flag, int q, int lane,
-                                              long long u_lo, int n_units, int t_first,
-                                              int i_first) {
+                                              int n_units) {
     using L = Lay<BITS, G>;
     using RM = RowMeta<L::kGPS>;
     const int r = 32 * q + lane;
     const uint32_t tl = tmem + (static_cast<uint32_t>(32 * q) << 16);
-    const bool vec = a.meta_vec != 0;
     bool dead = false;
     float acc[kN];
 #pragma unroll
     for (int j = 0; j < kN; ++j) acc[j] = 0.f;
     auto fail = [&]() {
-        record_error_tc(a, abort_flag);
+        record_error_tc(c.err, abort_flag);
         dead = true;
     };
 
-    int ft = t_first, fi = i_first;  // unit whose scales and zero points are fetched next
+    Cursor fc;  // unit whose scales and zero points are fetched next
+    fc.init(c);
+    Cursor cc = fc;  // unit being read back
     auto fetch = [&](RM& m) {
-        m.load(a, ft * kBN + r, static_cast<long long>(fi) * L::kGPS, vec);
-        if (++fi == a.I) {
-            fi = 0;
-            ++ft;
-        }
+        m.load(fc.v, fc.t * kBN + r, static_cast<long long>(fc.i) * L::kGPS);
+        fc.next(c);
     };
     Ring<L::kNA> as;
     Ring<L::kND> ds;
-    // Zero-point tiles of one batch of the current unit into A slot `as`.
+    // Zero-point tiles of one batch into A slot `as`.
     auto write_z = [&](auto bc, const RM& m) {
         constexpr int BB = decltype(bc)::value;
         constexpr int g_lo = BB == 0 ? 0 : L::kR0;
@@ -630,49 +779,72 @@ __device__ __forceinline__ void epilogue_warp(const GemmArgs& a, B& bars, uint32
         if (lane == 0) mbar_arrive(&bars.dfree[ds.slot]);
         ds.next();
     };
-    auto finish = [&](int tt, bool whole) {
-        if (!dead) finish_rows(a, acc, tt, whole, u_lo, r, q, lane);
-#pragma unroll
-        for (int j = 0; j < kN; ++j) acc[j] = 0.f;
-    };
 
     constexpr std::integral_constant<int, 0> kB0{};
     constexpr std::integral_constant<int, 1> kB1{};
-    RM cur, nxt, prev;
-    if (n_units > 0) fetch(cur);
-    int t = t_first, i = i_first;
-    int prev_t = 0;
-    bool prev_end = false, prev_whole = false;
-    for (int k = 0; k < n_units; ++k) {
-        if (k + 1 < n_units) fetch(nxt);
-        write_z(kB0, cur);
-        if (k > 0) {
-            read_d(kB1, prev);  // the previous unit's second batch
-            if (prev_end) finish(prev_t, prev_whole);
-        }
-        write_z(kB1, cur);
-        read_d(kB0, cur);
-        prev = cur;
-        prev_t = t;
-        prev_end = (i == a.I - 1) || (k == n_units - 1);
-        prev_whole = (i == a.I - 1) && (t != t_first || i_first == 0);
-        if (++i == a.I) {
-            i = 0;
-            ++t;
-        }
-        cur = nxt;
-    }
+    RM cur, nxt;
     if (n_units > 0) {
-        read_d(kB1, prev);
-        finish(prev_t, prev_whole);
+        fetch(cur);
+        write_z(kB0, cur);
+        write_z(kB1, cur);
+    }
+    bool seg_from_start = cc.i == 0;  // the open segment began at its tile's first k-stage
+    for (int k = 0; k < n_units; ++k) {
+        const bool more = k + 1 < n_units;
+        if (more) fetch(nxt);
+        read_d(kB0, cur);
+        if (more) {
+            write_z(kB0, nxt);
+            write_z(kB1, nxt);
+        }
+        read_d(kB1, cur);
+        // a tile segment ends with the tile or with the CTA's share of the phase
+        const bool tile_end = cc.i == cc.v.I - 1;
+        const bool end = tile_end || cc.last_of_share();
+        if (end) {
+            if (!dead) finish_rows(c, cc.v, cc.p, acc, cc.t, seg_from_start && tile_end, r, q, lane);
+#pragma unroll
+            for (int j = 0; j < kN; ++j) acc[j] = 0.f;
+        }
+        cc.next(c);
+        if (end) seg_from_start = cc.i == 0;
+        cur = nxt;
     }
     tc_fence_before();
 }
 
-template <int BITS, int G>
+// Producer's dependency check (fused step): true once projections 0..upto of
+// the launch are complete; `verified` caches how far that is known.
+__device__ __forceinline__ bool deps_ready(const Ctx& c, int upto, int& verified) {
+    bool acquired = false;
+    while (verified < upto) {
+        const int j = verified + 1;
+        if (ld_acquire_gpu(c.done + j) < 4 * c.proj[j].T) break;  // 4 lane quarters per tile
+        verified = j;
+        acquired = true;
+    }
+    // the TMA reads that follow are async-proxy accesses of data the acquire made visible
+    if (acquired) fence_proxy_async();
+    return verified >= upto;
+}
+
+// The same, waiting (bounded) until it holds.  Each poll is an L2 round
+// trip, so the loop needs no sleep.
+__device__ __forceinline__ bool wait_deps(const Ctx& c, int upto, int& verified,
+                                          volatile int* abort_flag) {
+    if (deps_ready(c, upto, verified)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t n = 1;; ++n) {
+        if (deps_ready(c, upto, verified)) return true;
+        if (*abort_flag) return false;
+        if ((n & 15u) == 0 && global_timer_ns() - t0 > kWaitLimitNs) return false;
+    }
+}
+
+template <int BITS, int G, bool MULTI>
 __global__ void __launch_bounds__(Lay<BITS, G>::kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-                   const GemmArgs a) {
+                   const GemmArgs a, const StepArgs sa) {
     using L = Lay<BITS, G>;
     constexpr int S = L::kStages;
     using BarsT = Bars<S, L::kNA, L::kND>;
@@ -682,6 +854,47 @@ __global__ void __launch_bounds__(Lay<BITS, G>::kThreads, 1)
     const uint32_t smem_u32 = smem_addr(smem);
     BarsT& bars = *reinterpret_cast<BarsT*>(smem + L::kBarOffset);
     volatile int* abort_flag = &bars.abort_flag;
+
+    Ctx c;
+    if constexpr (MULTI) {
+        c.proj = sa.proj;
+        c.phase = sa.phase;
+        c.nproj = sa.nproj;
+        c.nphase = sa.nphase;
+        c.partials = sa.partials;
+        c.counters = sa.counters;
+        c.done = sa.done;
+        c.err = sa.err;
+        c.U = sa.U;
+        c.P = sa.P;
+    } else {
+        c.proj = nullptr;
+        c.phase = nullptr;
+        c.nproj = 1;
+        c.nphase = 1;
+        c.one.tmW = &tmW;
+        c.one.tmX = &tmX;
+        c.one.scales = a.scales;
+        c.one.zeros = a.zeros;
+        c.one.y = a.y;
+        c.one.uoff = 0;
+        c.one.M = a.M;
+        c.one.N = a.N;
+        c.one.ng = a.ng;
+        c.one.T = a.T;
+        c.one.I = a.I;
+        c.one.toff = 0;
+        c.one.after = -1;
+        c.one.phase = 0;
+        c.one.meta_vec = a.meta_vec != 0;
+        c.one.x3d = a.x3d != 0;
+        c.partials = a.partials;
+        c.counters = a.counters;
+        c.done = nullptr;
+        c.err = a.err;
+        c.U = a.U;
+        c.P = a.P;
+    }
 
     // warp index through a shuffle so that the compiler treats it as uniform
     const int warp = __shfl_sync(kFull, static_cast<int>(threadIdx.x >> 5), 0);
@@ -701,6 +914,10 @@ __global__ void __launch_bounds__(Lay<BITS, G>::kThreads, 1)
         }
         mbar_init(&bars.drain, 1);
         *abort_flag = 0;
+        long long n = 0;
+        for (int ph = 0; ph < c.nphase; ++ph)
+            n += c.sub_lo(ph, blockIdx.x + 1) - c.sub_lo(ph, blockIdx.x);
+        bars.n_units = static_cast<int>(n);
         fence_mbar_init();
     }
     if (warp == L::kMmaWarp) {
@@ -712,32 +929,59 @@ __global__ void __launch_bounds__(Lay<BITS, G>::kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = bars.tmem_base;
 
-    const long long u_lo = a.U * blockIdx.x / a.P;
-    const long long u_hi = a.U * (blockIdx.x + 1) / a.P;
-    const int n_units = static_cast<int>(u_hi - u_lo);
-    const int t_first = static_cast<int>(u_lo / a.I);
-    const int i_first = static_cast<int>(u_lo - static_cast<long long>(t_first) * a.I);
+    const int n_units = bars.n_units;
     constexpr uint32_t kTail = 32 * (L::kUW + L::kEW + 1);  // warps that meet before dealloc
 
     if (warp == L::kProducerWarp) {
         // ------------------------------------------------------------ producer
         if (lane != 0) return;
-        prefetch_tensormap(&tmW);
-        prefetch_tensormap(&tmX);
         const uint64_t pol_w = policy_evict_first();
         const uint64_t pol_x = policy_evict_last();
-        int t = t_first, i = i_first;
-        uint32_t it = 0;
+        Cursor cu;
+        cu.init(c);
+        int maps_of = -1;   // projection whose tensor maps were last prefetched
+        int verified = -1;  // projections 0..verified of the launch known complete
+        // X loads held back until their projection's inputs are complete (fused
+        // step): the stage's packed words are loaded meanwhile.
+        constexpr int kQ = 8;
+        static_assert(S <= kQ, "pending queue holds a ring's worth of stages");
+        uint32_t q_slot[kQ];
+        const CUtensorMap* q_map[kQ];
+        int q_i[kQ], q_after[kQ], q_k[kQ];
+        bool q_x3d[kQ];
+        int q_head = 0, q_n = 0;
+        auto issue_x = [&](uint32_t slot, const CUtensorMap* map, int i, bool x3d) {
+            uint8_t* stage = smem + slot * L::kStageBytes;
+            if (x3d) {
+                tma_load_3d(stage + L::kWBytes, map, 0, 0, i * L::kXBoxes, &bars.full[slot], pol_x);
+            } else {
+#pragma unroll
+                for (int b = 0; b < L::kXBoxes; ++b)
+                    tma_load_2d(stage + L::kWBytes + b * L::kXBoxBytes, map,
+                                i * L::kStageValues + b * L::kXBoxValues, 0, &bars.full[slot], pol_x);
+            }
+        };
+        auto pop_x = [&]() {
+            issue_x(q_slot[q_head], q_map[q_head], q_i[q_head], q_x3d[q_head]);
+            q_head = (q_head + 1) % kQ;
+            --q_n;
+        };
         Ring<S> st;
+        uint32_t it = 0;
         bool ok = true;
         for (int k = 0; k < n_units; ++k, ++it) {
-            if (k == 0 || i == 0) {
+            if (cu.p != maps_of) {
+                prefetch_tensormap(cu.v.tmW);
+                prefetch_tensormap(cu.v.tmX);
+                maps_of = cu.p;
+            }
+            if (k == 0 || cu.i == 0) {
                 // warm L2 with the tile's scales and zero points (whole rows, rounded inward)
-                const int r0 = t * kBN, r1 = min(a.N, r0 + kBN);
-                const uintptr_t sb = reinterpret_cast<uintptr_t>(a.scales + static_cast<size_t>(r0) * a.ng);
-                const uintptr_t se = reinterpret_cast<uintptr_t>(a.scales + static_cast<size_t>(r1) * a.ng);
-                const uintptr_t zb = reinterpret_cast<uintptr_t>(a.zeros + static_cast<size_t>(r0) * a.ng);
-                const uintptr_t ze = reinterpret_cast<uintptr_t>(a.zeros + static_cast<size_t>(r1) * a.ng);
+                const int r0 = cu.t * kBN, r1 = min(cu.v.N, r0 + kBN);
+                const uintptr_t sb = reinterpret_cast<uintptr_t>(cu.v.scales + static_cast<size_t>(r0) * cu.v.ng);
+                const uintptr_t se = reinterpret_cast<uintptr_t>(cu.v.scales + static_cast<size_t>(r1) * cu.v.ng);
+                const uintptr_t zb = reinterpret_cast<uintptr_t>(cu.v.zeros + static_cast<size_t>(r0) * cu.v.ng);
+                const uintptr_t ze = reinterpret_cast<uintptr_t>(cu.v.zeros + static_cast<size_t>(r1) * cu.v.ng);
                 const uintptr_t sb16 = (sb + 15) & ~uintptr_t(15), se16 = se & ~uintptr_t(15);
                 const uintptr_t zb16 = (zb + 15) & ~uintptr_t(15), ze16 = ze & ~uintptr_t(15);
                 if (se16 > sb16)
@@ -745,8 +989,19 @@ __global__ void __launch_bounds__(Lay<BITS, G>::kThreads, 1)
                 if (ze16 > zb16)
                     prefetch_l2_bulk(reinterpret_cast<const void*>(zb16), static_cast<uint32_t>(ze16 - zb16));
             }
+            if constexpr (MULTI) {
+                // a held-back stage occupying the slot needed now cannot drain without its X
+                while (ok && q_n > 0 && q_k[q_head] <= k - S) {
+                    if (!wait_deps(c, q_after[q_head], verified, abort_flag)) ok = false;
+                    else pop_x();
+                }
+                if (!ok) {
+                    record_error_tc(c.err, abort_flag);
+                    break;
+                }
+            }
             if (!mbar_wait(&bars.empty[st.slot], st.phase ^ 1u, abort_flag)) {
-                record_error_tc(a, abort_flag);
+                record_error_tc(c.err, abort_flag);
                 ok = false;
                 break;
             }
@@ -755,21 +1010,37 @@ __global__ void __launch_bounds__(Lay<BITS, G>::kThreads, 1)
             mbar_arrive_expect_tx(fb, L::kWBytes + L::kXBytes);
 #pragma unroll
             for (int b = 0; b < L::kBoxes; ++b)
-                tma_load_2d(stage + b * L::kBoxBytes, &tmW, (i * L::kBoxes + b) * kWordsPerStage,
-                            t * kBN, fb, pol_w);
-            if (a.x3d) {
-                tma_load_3d(stage + L::kWBytes, &tmX, 0, 0, i * L::kXBoxes, fb, pol_x);
+                tma_load_2d(stage + b * L::kBoxBytes, cu.v.tmW, (cu.i * L::kBoxes + b) * kWordsPerStage,
+                            cu.t * kBN, fb, pol_w);
+            if (!MULTI || cu.v.after < 0 || (q_n == 0 && deps_ready(c, cu.v.after, verified))) {
+                issue_x(st.slot, cu.v.tmX, cu.i, cu.v.x3d);
             } else {
-#pragma unroll
-                for (int b = 0; b < L::kXBoxes; ++b)
-                    tma_load_2d(stage + L::kWBytes + b * L::kXBoxBytes, &tmX,
-                                i * L::kStageValues + b * L::kXBoxValues, 0, fb, pol_x);
+                const int e = (q_head + q_n) % kQ;
+                q_slot[e] = st.slot;
+                q_map[e] = cu.v.tmX;
+                q_i[e] = cu.i;
+                q_x3d[e] = cu.v.x3d;
+                q_after[e] = cu.v.after;
+                q_k[e] = k;
+                ++q_n;
             }
-            if (++i == a.I) {
-                i = 0;
-                ++t;
-            }
+            if constexpr (MULTI)
+                while (q_n > 0 && deps_ready(c, q_after[q_head], verified)) pop_x();
+            cu.next(c);
             st.next();
+        }
+        if constexpr (MULTI) {
+            while (ok && q_n > 0) {
+                if (!wait_deps(c, q_after[q_head], verified, abort_flag)) {
+                    record_error_tc(c.err, abort_flag);
+                    ok = false;
+                } else {
+                    pop_x();
+                }
+            }
+            // on failure: issue what was held back (the results are discarded)
+            // so that every stage in flight completes before shared memory goes away
+            while (q_n > 0) pop_x();
         }
         if (!ok) {
             // let copies already in flight land before the CTA's shared memory goes away
@@ -830,7 +1101,7 @@ __global__ void __launch_bounds__(Lay<BITS, G>::kThreads, 1)
             });
             st.next();
         }
-        if (!ok && lane == 0) record_error_tc(a, abort_flag);
+        if (!ok && lane == 0) record_error_tc(c.err, abort_flag);
         // every MMA issued above has completed once `drain` flips
         if (elect_one()) tc_commit(&bars.drain);
         __syncwarp();
@@ -844,19 +1115,16 @@ __global__ void __launch_bounds__(Lay<BITS, G>::kThreads, 1)
 
     if (warp >= L::kUW) {
         // ------------------------------------------------------------ epilogue
-        epilogue_warp<BITS, G>(a, bars, tmem, abort_flag, warp & 3, lane, u_lo, n_units, t_first,
-                               i_first);
+        epilogue_warp<BITS, G>(c, bars, tmem, abort_flag, warp & 3, lane, n_units);
     } else if constexpr (BITS == 3) {
         // ------------------------------------------------------------ unpack
         static_for<0, L::kSplit>([&](auto hc) {
             constexpr int H = decltype(hc)::value;
             if ((warp >> 2) == H)
-                unpack_warp<BITS, G, H>(a, smem_u32, bars, tmem, abort_flag, warp, lane, n_units,
-                                        t_first, i_first);
+                unpack_warp<BITS, G, H>(c, smem_u32, bars, tmem, abort_flag, warp, lane, n_units);
         });
     } else {
-        unpack_warp<BITS, G, -1>(a, smem_u32, bars, tmem, abort_flag, warp, lane, n_units, t_first,
-                                 i_first);
+        unpack_warp<BITS, G, -1>(c, smem_u32, bars, tmem, abort_flag, warp, lane, n_units);
     }
     named_bar_sync(3, kTail);
 }
@@ -865,12 +1133,36 @@ template <int BITS, int G>
 cudaError_t launch_tc(const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmArgs& a,
                       cudaStream_t s) {
     using L = Lay<BITS, G>;
-    auto kern = gemm_tc_kernel<BITS, G>;
+    auto kern = gemm_tc_kernel<BITS, G, false>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
     if (e != cudaSuccess) return e;
-    kern<<<a.P, L::kThreads, L::kSmemBytes, s>>>(tmW, tmX, a);
+    kern<<<a.P, L::kThreads, L::kSmemBytes, s>>>(tmW, tmX, a, StepArgs{});
     return cudaGetLastError();
+}
+
+// Fused step launch; cooperative (all CTAs resident at once) when projections
+// wait for one another.
+template <int BITS, int G>
+cudaError_t launch_step(const StepArgs& sa, bool cooperative, cudaStream_t s) {
+    using L = Lay<BITS, G>;
+    auto kern = gemm_tc_kernel<BITS, G, true>;
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    CUtensorMap none{};
+    GemmArgs a{};
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(sa.P));
+    cfg.blockDim = dim3(L::kThreads);
+    cfg.dynamicSmemBytes = L::kSmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = cooperative ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, none, none, a, sa);
 }
 
 }  // namespace tc

@@ -5,6 +5,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "wq.h"
+
 namespace wq {
 
 constexpr int kBN = 128;              // weight rows per tile (TMEM lanes)
@@ -40,6 +42,46 @@ struct GemmArgs {
     int x3d;          // X map is 3-D [K/64][M][64]: one TMA box per stage (K % 64 == 0)
 };
 
+// One projection of a fused step, as the step kernel reads it from device
+// memory.  Units of all projections form one space: projection p owns global
+// units [uoff, uoff + T * I) and global tiles [toff, toff + T).
+struct ProjDev {  // aligned like its tensor maps
+    CUtensorMap tmW;         // packed words [N][W]
+    CUtensorMap tmX;         // X [M][K] (3-D map when x3d)
+    const uint16_t* scales;  // [N][ng] bf16
+    const uint8_t* zeros;    // [N][ng]
+    float* y;                // [M][N]
+    long long uoff;          // first global unit
+    int M, N, ng, T, I;
+    int toff;                // first global tile
+    int meta_vec, x3d;
+    int after;               // X is read once projections 0..after of this launch are complete (-1: at once)
+    int phase;               // phase of the launch this projection belongs to
+    int pad[4];
+};
+
+// A phase of a fused step: consecutive projections none of which waits for
+// another projection of the phase.  Every CTA takes its stream-K share of
+// every phase: units [uoff + U b / P, uoff + U (b + 1) / P).
+struct PhaseDev {
+    long long uoff;  // first global unit
+    long long U;     // units of the phase
+};
+static_assert(sizeof(ProjDev) % 64 == 0, "ProjDev keeps 64-byte alignment in arrays");
+
+// Kernel-wide arguments of a fused step launch.
+struct StepArgs {
+    const ProjDev* proj;    // [nproj]
+    const PhaseDev* phase;  // [nphase]
+    int nproj, nphase;
+    float* partials;      // [2 * P][kMaxCols][kBN]
+    int* counters;        // [total tiles][kCountersPerTile]
+    int* done;            // [nproj] finished (tile, lane quarter) pairs, zero at launch
+    int* err;
+    long long U;          // total units
+    int P;
+};
+
 // Static stream-K schedule: CTA b owns units [unit_begin(b), unit_begin(b+1)).
 inline long long unit_begin(long long U, int P, int b) { return U * b / P; }
 
@@ -53,6 +95,21 @@ cudaError_t launch_gemm_tc_b3(int group, const CUtensorMap& tmW, const CUtensorM
                               const GemmArgs& a, cudaStream_t s);
 cudaError_t launch_gemm_tc_b2(int group, const CUtensorMap& tmW, const CUtensorMap& tmX,
                               const GemmArgs& a, cudaStream_t s);
+// Fused step: all projections of `sa` (one bit width and group size) in one
+// persistent launch; cooperative when any projection waits for another.
+cudaError_t launch_step_b4(int group, const StepArgs& sa, bool cooperative, cudaStream_t s);
+cudaError_t launch_step_b3(int group, const StepArgs& sa, bool cooperative, cudaStream_t s);
+cudaError_t launch_step_b2(int group, const StepArgs& sa, bool cooperative, cudaStream_t s);
+
+// Host helpers shared by the entry points (wq_api.cu).
+wq_status_t host_cuda_fail(cudaError_t e);
+wq_status_t host_sm_count(int* sms);
+wq_status_t host_check_gemm(const uint16_t* x, const uint32_t* wq, const uint16_t* scales,
+                            const uint8_t* zeros, const float* y, int M, int N, int K, int group,
+                            int bits);
+wq_status_t host_encode_proj(const uint16_t* x, const uint32_t* wq, const uint16_t* scales,
+                             const uint8_t* zeros, int M, int N, int K, int group, int bits,
+                             CUtensorMap* tmW, CUtensorMap* tmX, int* x3d, int* meta_vec);
 
 // Elementwise kernels.
 cudaError_t launch_pack(const uint8_t* q, uint32_t* wq, int N, int K, int bits, int W,

@@ -1,54 +1,333 @@
-// Decode-step driver: a layer stack's projections back to back on one stream
-// (OpenJet news page, paragraph "并行解码的原理": every projection of every
-// layer streams its packed weights once per step).  The launch sequence can be
-// captured once into a CUDA graph so a step costs one graph launch on the host.
+// Decode-step driver: a layer stack's projections on one stream (OpenJet news
+// page, paragraph "并行解码的原理": every projection of every layer streams its
+// packed weights once per step; the whole step runs as one persistent kernel
+// with no per-layer launch).
+//
+// Sequential mode launches wq_gemm once per projection.  Fused mode builds a
+// table of projections (tensor maps, pointers, unit and tile offsets) and
+// launches one persistent kernel per run of consecutive projections with the
+// same bit width and group size; the kernel streams the units of the whole
+// run, and a projection whose X depends on earlier ones waits for them on
+// device-side completion counters while its packed weights are already being
+// loaded.  Either sequence can be captured once into a CUDA graph.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <new>
+#include <vector>
 
 #include "wq.h"
+#include "wq_internal.h"
 
-struct wq_step_graph {
-    cudaGraph_t graph = nullptr;
-    cudaGraphExec_t exec = nullptr;
+namespace {
+
+size_t round256(size_t v) { return (v + 255) / 256 * 256; }
+
+// A run: projections [begin, end) of one bit width and group size, all with
+// M, N, K > 0 (other projections run through wq_gemm on their own).
+struct Run {
+    int begin, end, bits, group;
+    bool fused;
 };
 
-extern "C" {
+std::vector<Run> split_runs(const wq_proj_desc_t* projs, int count) {
+    std::vector<Run> runs;
+    for (int i = 0; i < count; ++i) {
+        const wq_proj_desc_t& p = projs[i];
+        const bool fusable = p.M > 0 && p.N > 0 && p.K > 0;
+        if (fusable && !runs.empty() && runs.back().fused && runs.back().end == i &&
+            runs.back().bits == p.bits && runs.back().group == p.group) {
+            runs.back().end = i + 1;
+        } else {
+            runs.push_back({i, i + 1, p.bits, p.group, fusable});
+        }
+    }
+    return runs;
+}
 
-wq_status_t wq_step_run(const wq_proj_desc_t* projs, int count, void* workspace,
-                        size_t workspace_bytes, void* stream) {
+// Fused-mode workspace layout, shared by every run of a step (runs execute
+// one after another in stream order).
+struct FusedLayout {
+    size_t partial_off, counter_off, done_off, table_off, bytes;
+};
+
+int tiles_of(const wq_proj_desc_t& p) { return (p.N + wq::kBN - 1) / wq::kBN; }
+
+// Device tables of a step: one projection slot and one phase slot per
+// projection; run r uses the slots starting at its first projection.
+size_t table_bytes(int count) {
+    return static_cast<size_t>(count) * (sizeof(wq::ProjDev) + sizeof(wq::PhaseDev));
+}
+struct Tables {
+    wq::ProjDev* proj;
+    wq::PhaseDev* phase;
+};
+Tables tables_at(void* base, int count) {
+    Tables t;
+    t.proj = static_cast<wq::ProjDev*>(base);
+    t.phase = reinterpret_cast<wq::PhaseDev*>(t.proj + count);
+    return t;
+}
+
+FusedLayout fused_layout(const wq_proj_desc_t* projs, int count, const std::vector<Run>& runs,
+                         int sms) {
+    size_t max_tiles = 0, max_count = 0;
+    for (const Run& r : runs) {
+        if (!r.fused) continue;
+        size_t t = 0;
+        for (int i = r.begin; i < r.end; ++i) t += static_cast<size_t>(tiles_of(projs[i]));
+        max_tiles = std::max(max_tiles, t);
+        max_count = std::max(max_count, static_cast<size_t>(r.end - r.begin));
+    }
+    FusedLayout l;
+    l.partial_off = wq::kWsHeader;
+    l.counter_off = l.partial_off +
+                    round256(size_t(2) * sms * wq::kMaxCols * wq::kBN * sizeof(float));
+    l.done_off = l.counter_off + round256(max_tiles * wq::kCountersPerTile * sizeof(int));
+    l.table_off = l.done_off + round256(max_count * sizeof(int));
+    l.bytes = l.table_off + round256(table_bytes(count));
+    return l;
+}
+
+wq_status_t check_all(const wq_proj_desc_t* projs, int count) {
     if (count < 0 || (count > 0 && !projs)) return WQ_ERR_INVALID_ARG;
     for (int i = 0; i < count; ++i) {
         const wq_proj_desc_t& p = projs[i];
-        wq_status_t st = wq_gemm(p.x, p.wq, p.scales, p.zeros, p.y, p.M, p.N, p.K, p.group, p.bits,
-                                 workspace, workspace_bytes, stream);
-        if (st != WQ_OK) return st;
+        if (wq_status_t st = wq::host_check_gemm(p.x, p.wq, p.scales, p.zeros, p.y, p.M, p.N, p.K,
+                                                 p.group, p.bits))
+            return st;
+        if (p.after >= i || p.after < -1) return WQ_ERR_INVALID_ARG;
     }
     return WQ_OK;
 }
 
-wq_status_t wq_step_graph_create(const wq_proj_desc_t* projs, int count, void* workspace,
-                                 size_t workspace_bytes, void* stream, wq_step_graph_t* out) {
+// Host-side tables of one run.  The run is cut into phases: a projection
+// that waits for a projection of the current phase starts a new phase, and
+// every projection of a later phase then waits for all earlier phases (its X
+// is held back; its packed weights still stream).  Returns the total units and
+// whether anything waits.
+wq_status_t build_table(const wq_proj_desc_t* projs, const Run& r, std::vector<wq::ProjDev>& out,
+                        std::vector<wq::PhaseDev>& phases, long long* units, bool* waits) {
+    out.assign(static_cast<size_t>(r.end - r.begin), wq::ProjDev{});
+    phases.clear();
+    long long uoff = 0;
+    int toff = 0;
+    int phase_start = 0;  // first projection (run-relative) of the current phase
+    *waits = false;
+    const int sv = wq::tc_stage_values(r.bits, r.group);
+    for (int i = r.begin; i < r.end; ++i) {
+        const wq_proj_desc_t& p = projs[i];
+        const int li = i - r.begin;
+        wq::ProjDev& d = out[static_cast<size_t>(li)];
+        if (wq_status_t st = wq::host_encode_proj(p.x, p.wq, p.scales, p.zeros, p.M, p.N, p.K,
+                                                  p.group, p.bits, &d.tmW, &d.tmX, &d.x3d,
+                                                  &d.meta_vec))
+            return st;
+        // a producer before this run is complete by stream order
+        const int after = p.after >= r.begin ? p.after - r.begin : -1;
+        if (li == 0 || after >= phase_start) {
+            if (li > 0) *waits = true;
+            phase_start = li;
+            phases.push_back({uoff, 0});
+        }
+        d.scales = p.scales;
+        d.zeros = p.zeros;
+        d.y = p.y;
+        d.M = p.M;
+        d.N = p.N;
+        d.ng = p.K / p.group;
+        d.T = tiles_of(p);
+        d.I = (p.K + sv - 1) / sv;
+        d.uoff = uoff;
+        d.toff = toff;
+        d.phase = static_cast<int>(phases.size()) - 1;
+        d.after = phase_start > 0 ? phase_start - 1 : -1;
+        const long long u = static_cast<long long>(d.T) * d.I;
+        phases.back().U += u;
+        uoff += u;
+        toff += d.T;
+    }
+    *units = uoff;
+    return WQ_OK;
+}
+
+// Reset the run's completion counters and launch its persistent kernel.
+wq_status_t launch_run(const Run& r, Tables tab, int nphase, long long units, bool waits,
+                       uint8_t* ws, const FusedLayout& lay, int sms, cudaStream_t s) {
+    const int n = r.end - r.begin;
+    int* done = reinterpret_cast<int*>(ws + lay.done_off);
+    cudaError_t e = cudaMemsetAsync(done, 0, static_cast<size_t>(n) * sizeof(int), s);
+    if (e != cudaSuccess) return wq::host_cuda_fail(e);
+    wq::StepArgs sa;
+    sa.proj = tab.proj + r.begin;
+    sa.phase = tab.phase + r.begin;
+    sa.nproj = n;
+    sa.nphase = nphase;
+    sa.partials = reinterpret_cast<float*>(ws + lay.partial_off);
+    sa.counters = reinterpret_cast<int*>(ws + lay.counter_off);
+    sa.done = done;
+    sa.err = reinterpret_cast<int*>(ws);
+    sa.U = units;
+    sa.P = static_cast<int>(std::min<long long>(sms, units));
+    if (r.bits == 4)
+        e = wq::launch_step_b4(r.group, sa, waits, s);
+    else if (r.bits == 3)
+        e = wq::launch_step_b3(r.group, sa, waits, s);
+    else
+        e = wq::launch_step_b2(r.group, sa, waits, s);
+    return e == cudaSuccess ? WQ_OK : wq::host_cuda_fail(e);
+}
+
+wq_status_t run_single(const wq_proj_desc_t& p, void* workspace, size_t workspace_bytes,
+                       cudaStream_t s) {
+    return wq_gemm(p.x, p.wq, p.scales, p.zeros, p.y, p.M, p.N, p.K, p.group, p.bits, workspace,
+                   workspace_bytes, s);
+}
+
+// Upload every run's tables to `base` (table_bytes(count) of device memory),
+// synchronously: graphs do this once before capturing.
+wq_status_t upload_tables(const wq_proj_desc_t* projs, int count, void* base) {
+    const Tables tab = tables_at(base, count);
+    std::vector<wq::ProjDev> host;
+    std::vector<wq::PhaseDev> phases;
+    for (const Run& r : split_runs(projs, count)) {
+        if (!r.fused) continue;
+        long long units = 0;
+        bool waits = false;
+        if (wq_status_t st = build_table(projs, r, host, phases, &units, &waits)) return st;
+        cudaError_t e = cudaMemcpy(tab.proj + r.begin, host.data(),
+                                   host.size() * sizeof(wq::ProjDev), cudaMemcpyHostToDevice);
+        if (e == cudaSuccess)
+            e = cudaMemcpy(tab.phase + r.begin, phases.data(), phases.size() * sizeof(wq::PhaseDev),
+                           cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) return wq::host_cuda_fail(e);
+    }
+    return WQ_OK;
+}
+
+// Fused step.  With `tables` (device, uploaded by upload_tables) the launches
+// read those; without, each run's tables are staged into the workspace's
+// table area (slots per projection, so no run overwrites another's) first.
+wq_status_t run_fused(const wq_proj_desc_t* projs, int count, void* workspace,
+                      size_t workspace_bytes, cudaStream_t s, void* tables) {
+    int sms = 0;
+    if (wq_status_t st = wq::host_sm_count(&sms)) return st;
+    const std::vector<Run> runs = split_runs(projs, count);
+    const FusedLayout lay = fused_layout(projs, count, runs, sms);
+    if (!workspace || workspace_bytes < lay.bytes ||
+        reinterpret_cast<uintptr_t>(workspace) % 16 != 0)
+        return WQ_ERR_INVALID_ARG;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    const Tables tab = tables_at(tables ? tables : ws + lay.table_off, count);
+    std::vector<wq::ProjDev> host;
+    std::vector<wq::PhaseDev> phases;
+    for (const Run& r : runs) {
+        if (!r.fused) {
+            if (wq_status_t st = run_single(projs[r.begin], workspace, workspace_bytes, s)) return st;
+            continue;
+        }
+        long long units = 0;
+        bool waits = false;
+        if (wq_status_t st = build_table(projs, r, host, phases, &units, &waits)) return st;
+        if (!tables) {
+            // pageable sources: each copy is staged before the call returns
+            cudaError_t e = cudaMemcpyAsync(tab.proj + r.begin, host.data(),
+                                            host.size() * sizeof(wq::ProjDev),
+                                            cudaMemcpyHostToDevice, s);
+            if (e == cudaSuccess)
+                e = cudaMemcpyAsync(tab.phase + r.begin, phases.data(),
+                                    phases.size() * sizeof(wq::PhaseDev), cudaMemcpyHostToDevice, s);
+            if (e != cudaSuccess) return wq::host_cuda_fail(e);
+        }
+        if (wq_status_t st = launch_run(r, tab, static_cast<int>(phases.size()), units, waits, ws,
+                                        lay, sms, s))
+            return st;
+    }
+    return WQ_OK;
+}
+
+}  // namespace
+
+struct wq_step_graph {
+    cudaGraph_t graph = nullptr;
+    cudaGraphExec_t exec = nullptr;
+    void* tables = nullptr;  // fused mode: device copy of every run's tables
+};
+
+extern "C" {
+
+size_t wq_step_workspace_bytes(const wq_proj_desc_t* projs, int count, unsigned flags) {
+    if (check_all(projs, count) != WQ_OK) return 0;
+    size_t need = wq::kWsHeader;
+    for (int i = 0; i < count; ++i) {
+        const wq_proj_desc_t& p = projs[i];
+        need = std::max(need, wq_workspace_bytes(p.M, p.N, p.K, p.group, p.bits));
+    }
+    if (flags & WQ_STEP_FUSED) {
+        int sms = 0;
+        if (wq::host_sm_count(&sms) != WQ_OK) return 0;
+        need = std::max(need, fused_layout(projs, count, split_runs(projs, count), sms).bytes);
+    }
+    return need;
+}
+
+wq_status_t wq_step_run_ex(const wq_proj_desc_t* projs, int count, unsigned flags,
+                           void* workspace, size_t workspace_bytes, void* stream) {
+    if (wq_status_t st = check_all(projs, count)) return st;
+    if (flags & ~WQ_STEP_FUSED) return WQ_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (flags & WQ_STEP_FUSED) return run_fused(projs, count, workspace, workspace_bytes, s, nullptr);
+    for (int i = 0; i < count; ++i)
+        if (wq_status_t st = run_single(projs[i], workspace, workspace_bytes, s)) return st;
+    return WQ_OK;
+}
+
+wq_status_t wq_step_run(const wq_proj_desc_t* projs, int count, void* workspace,
+                        size_t workspace_bytes, void* stream) {
+    return wq_step_run_ex(projs, count, 0u, workspace, workspace_bytes, stream);
+}
+
+wq_status_t wq_step_graph_create_ex(const wq_proj_desc_t* projs, int count, unsigned flags,
+                                    void* workspace, size_t workspace_bytes, void* stream,
+                                    wq_step_graph_t* out) {
     if (!out || !workspace || count <= 0 || !projs) return WQ_ERR_INVALID_ARG;
     *out = nullptr;
+    if (wq_status_t st = check_all(projs, count)) return st;
+    if (flags & ~WQ_STEP_FUSED) return WQ_ERR_INVALID_ARG;
+    wq_step_graph* g = new (std::nothrow) wq_step_graph;
+    if (!g) return WQ_ERR_CUDA;
+    wq_status_t st = WQ_OK;
+    if (flags & WQ_STEP_FUSED) {
+        cudaError_t e = cudaMalloc(&g->tables, table_bytes(count));
+        if (e != cudaSuccess) st = wq::host_cuda_fail(e);
+        if (st == WQ_OK) st = upload_tables(projs, count, g->tables);
+    }
     // Capture needs a non-legacy stream: use the caller's, or a private one.
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaStream_t own = nullptr;
-    if (s == nullptr) {
-        if (cudaStreamCreateWithFlags(&own, cudaStreamNonBlocking) != cudaSuccess) return WQ_ERR_CUDA;
+    if (st == WQ_OK && s == nullptr) {
+        if (cudaStreamCreateWithFlags(&own, cudaStreamNonBlocking) != cudaSuccess) st = WQ_ERR_CUDA;
         s = own;
     }
-    wq_step_graph* g = new (std::nothrow) wq_step_graph;
-    wq_status_t st = g ? WQ_OK : WQ_ERR_CUDA;
     if (st == WQ_OK && cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal) != cudaSuccess)
         st = WQ_ERR_CUDA;
     if (st == WQ_OK) {
-        wq_status_t run = wq_step_run(projs, count, workspace, workspace_bytes, s);
+        wq_status_t run;
+        if (flags & WQ_STEP_FUSED) {
+            run = run_fused(projs, count, workspace, workspace_bytes, s, g->tables);
+        } else {
+            run = WQ_OK;
+            for (int i = 0; i < count && run == WQ_OK; ++i)
+                run = run_single(projs[i], workspace, workspace_bytes, s);
+        }
         cudaError_t e = cudaStreamEndCapture(s, &g->graph);
         if (run != WQ_OK) st = run;
-        else if (e != cudaSuccess) st = WQ_ERR_CUDA;
+        else if (e != cudaSuccess) st = wq::host_cuda_fail(e);
     }
-    if (st == WQ_OK && cudaGraphInstantiate(&g->exec, g->graph, 0) != cudaSuccess) st = WQ_ERR_CUDA;
+    if (st == WQ_OK) {
+        cudaError_t e = cudaGraphInstantiate(&g->exec, g->graph, 0);
+        if (e != cudaSuccess) st = wq::host_cuda_fail(e);
+    }
     if (own) cudaStreamDestroy(own);
     if (st != WQ_OK) {
         wq_step_graph_destroy(g);
@@ -56,6 +335,11 @@ wq_status_t wq_step_graph_create(const wq_proj_desc_t* projs, int count, void* w
     }
     *out = g;
     return WQ_OK;
+}
+
+wq_status_t wq_step_graph_create(const wq_proj_desc_t* projs, int count, void* workspace,
+                                 size_t workspace_bytes, void* stream, wq_step_graph_t* out) {
+    return wq_step_graph_create_ex(projs, count, 0u, workspace, workspace_bytes, stream, out);
 }
 
 wq_status_t wq_step_graph_launch(wq_step_graph_t g, void* stream) {
@@ -69,6 +353,7 @@ void wq_step_graph_destroy(wq_step_graph_t g) {
     if (!g) return;
     if (g->exec) cudaGraphExecDestroy(g->exec);
     if (g->graph) cudaGraphDestroy(g->graph);
+    if (g->tables) cudaFree(g->tables);
     delete g;
 }
 
