@@ -46,7 +46,7 @@ namespace tc {
 
 constexpr int kN = 16;  // MMA N: rows of X (M padded to 16)
 constexpr uint32_t kTmemCols = 512;
-constexpr int kSmemBudgetTc = 210 * 1024;
+constexpr int kSmemBudgetTc = 220 * 1024;
 // Unpack warps per TMEM lane quarter (each takes 1 / kSplitWarps of a
 // group's K steps): two per lane quarter measured best; more add per-warp
 // overhead without adding ALU throughput.
@@ -87,8 +87,15 @@ struct Lay {
     static constexpr int kXBoxes = kStageValues / kXBoxValues;
     static constexpr int kXBoxBytes = kN * 128;                 // 16 rows x 128 bytes
     static constexpr int kXBytes = kXBoxes * kXBoxBytes;
-    static constexpr int kStageBytes = round_up_tc(kWBytes + kXBytes, 1024);
     static constexpr int kGPS = kStageValues / G;               // groups per stage
+    // The stage also carries its rows' zero points, kZRow bytes per row (kGPS
+    // rounded up to 4, 8 or 16 bytes for aligned shared loads), staged by the
+    // producer warp.
+    static constexpr int kZRow = kGPS <= 4 ? 4 : kGPS <= 8 ? 8 : 16;
+    static constexpr int kZOff = kWBytes + kXBytes;
+    static constexpr int kZStageBytes = kBN * kZRow;
+    static constexpr bool kZAsync = kZRow == kGPS && (kZRow == 4 || kZRow == 8 || kZRow == 16);
+    static constexpr int kStageBytes = round_up_tc(kWBytes + kXBytes + kZStageBytes, 1024);
     static constexpr int kSteps = G / 16;                       // K16 steps per group
     static constexpr int kACols = kSteps * 8;                   // TMEM columns of one A tile
     // Warp roles: kUW unpack warps (kSplit per TMEM lane quarter, each taking
@@ -202,6 +209,38 @@ struct RowMeta {
                 z[gi / 4] |= static_cast<uint32_t>(__ldg(a.zeros + base + gi)) << (8 * (gi & 3));
             }
         }
+    }
+
+    // Zero points only (the unpack warps need nothing else).
+    template <class V>
+    __device__ __forceinline__ void load_z(const V& a, int n, long long g0) {
+#pragma unroll
+        for (int j = 0; j < kZ; ++j) z[j] = 0;
+        if (n >= a.N) return;
+        const long long base = static_cast<long long>(n) * a.ng + g0;
+        if constexpr (GPS == 4 || GPS == 8 || GPS == 16) {
+            if (a.meta_vec) {
+                const uint8_t* zp = a.zeros + base;
+                if constexpr (GPS == 4) {
+                    z[0] = __ldg(reinterpret_cast<const uint32_t*>(zp));
+                } else if constexpr (GPS == 8) {
+                    const uint2 w = __ldg(reinterpret_cast<const uint2*>(zp));
+                    z[0] = w.x;
+                    z[1] = w.y;
+                } else {
+                    const uint4 w = __ldg(reinterpret_cast<const uint4*>(zp));
+                    z[0] = w.x;
+                    z[1] = w.y;
+                    z[2] = w.z;
+                    z[3] = w.w;
+                }
+                return;
+            }
+        }
+#pragma unroll
+        for (int gi = 0; gi < GPS; ++gi)
+            if (g0 + gi < a.ng)
+                z[gi / 4] |= static_cast<uint32_t>(__ldg(a.zeros + base + gi)) << (8 * (gi & 3));
     }
 
     __device__ __forceinline__ float scale(int gi) const {
@@ -603,7 +642,7 @@ template <int S, int NA, int ND>
 struct Bars {
     uint64_t full[S];    // stage landed (TMA transaction bytes)
     uint64_t empty[S];   // stage consumed: unpack warps + one MMA commit
-    uint64_t filled[NA]; // A slot written (unpack warps, and epilogue warps for zero-point tiles)
+    uint64_t filled[NA]; // A slot written (unpack warps)
     uint64_t afree[NA];  // A slot's MMAs complete (tcgen05.commit)
     uint64_t dfull[ND];  // accumulator slot's MMAs complete (tcgen05.commit)
     uint64_t dfree[ND];  // accumulator slot read back (epilogue warps)
@@ -640,16 +679,6 @@ __device__ __forceinline__ void unpack_warp(const Ctx& c, uint32_t smem_u32, B& 
     const uint32_t row_off = static_cast<uint32_t>(r * 128) | (static_cast<uint32_t>(lane & 7) << 4);
     bool dead = false;  // after a failed wait: no more shared or tensor memory work
 
-    // Zero points are needed here only when they are subtracted on the CUDA
-    // cores; otherwise the epilogue warps write the zero-point tiles.
-    Cursor fc;
-    if constexpr (!L::kZtc) fc.init(c);
-    auto fetch = [&](RM& m) {
-        if constexpr (!L::kZtc) {
-            m.load(fc.v, fc.t * kBN + r, static_cast<long long>(fc.i) * L::kGPS);
-            fc.next(c);
-        }
-    };
     auto fail = [&]() {
         record_error_tc(c.err, abort_flag);
         dead = true;
@@ -657,11 +686,27 @@ __device__ __forceinline__ void unpack_warp(const Ctx& c, uint32_t smem_u32, B& 
 
     Ring<L::kStages> st;
     Ring<L::kNA> as;
-    RM cur, nxt;
-    if (n_units > 0) fetch(cur);
+    RM cur;
     for (int k = 0; k < n_units; ++k) {
-        if (k + 1 < n_units) fetch(nxt);
         if (!dead && !wait_all(&bars.full[st.slot], st.phase, abort_flag)) fail();
+        // the unit's zero points, staged with its words
+        {
+            const uint32_t zs = smem_u32 + st.slot * L::kStageBytes + L::kZOff + r * L::kZRow;
+            if constexpr (RM::kZ == 1) {
+                cur.z[0] = lds32(zs);
+            } else if constexpr (RM::kZ == 2) {
+                const uint2 v = lds64(zs);
+                cur.z[0] = v.x;
+                cur.z[RM::kZ > 1 ? 1 : 0] = v.y;
+            } else {
+                static_assert(RM::kZ <= 4, "zero points per row");
+                const uint4 v = lds128(zs);
+                cur.z[0] = v.x;
+                if constexpr (RM::kZ > 1) cur.z[1] = v.y;
+                if constexpr (RM::kZ > 2) cur.z[2] = v.z;
+                if constexpr (RM::kZ > 3) cur.z[3] = v.w;
+            }
+        }
         // Both A slots of this stage must have left the tensor core: the MMAs
         // complete in order, so waiting for the later slot's previous batch
         // covers the earlier one.
@@ -682,6 +727,11 @@ __device__ __forceinline__ void unpack_warp(const Ctx& c, uint32_t smem_u32, B& 
                         write_group<BITS, G, HT, GI>(row_sw, tA, cur);
                     else
                         write_group_rt<BITS, G, GI>(row_sw, tA, cur, h);
+                    // the group's zero-point tile, from one of the lane quarter's warps
+                    if constexpr (L::kZtc)
+                        if (GI % L::kSplit == h)
+                            tmem_st8_same(tl + L::kColZ + (as.slot * L::kR0 + (GI - g_lo)) * 8,
+                                          cur.neg_zero_point(GI));
                 });
                 tmem_wait_st();
                 tc_fence_before();
@@ -692,15 +742,13 @@ __device__ __forceinline__ void unpack_warp(const Ctx& c, uint32_t smem_u32, B& 
         });
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars.empty[st.slot]);  // the stage's words are no longer needed
-        cur = nxt;
         st.next();
     }
 }
 
 // Epilogue warp (lane quarter q).  Per unit it reads the unit's two batches
-// of accumulators back (adding scale * D to the row's 16 fp32 sums), writes
-// the next unit's zero-point tiles (when the zero point is applied on the
-// tensor core) in between, and ends tile segments.
+// of accumulators back (adding scale * D to the row's 16 fp32 sums) and ends
+// tile segments.
 template <int BITS, int G, class B>
 __device__ __forceinline__ void epilogue_warp(const Ctx& c, B& bars, uint32_t tmem,
                                               volatile int* abort_flag, int q, int lane,
@@ -725,29 +773,7 @@ __device__ __forceinline__ void epilogue_warp(const Ctx& c, B& bars, uint32_t tm
         m.load(fc.v, fc.t * kBN + r, static_cast<long long>(fc.i) * L::kGPS);
         fc.next(c);
     };
-    Ring<L::kNA> as;
     Ring<L::kND> ds;
-    // Zero-point tiles of one batch into A slot `as`.
-    auto write_z = [&](auto bc, const RM& m) {
-        constexpr int BB = decltype(bc)::value;
-        constexpr int g_lo = BB == 0 ? 0 : L::kR0;
-        constexpr int g_hi = BB == 0 ? L::kR0 : L::kGPS;
-        if constexpr (L::kZtc) {
-            if (!dead && !wait_all(&bars.afree[as.slot], as.phase ^ 1u, abort_flag)) fail();
-            if (!dead) {
-                static_for<g_lo, g_hi>([&](auto gc) {
-                    constexpr int GI = decltype(gc)::value;
-                    tmem_st8_same(tl + L::kColZ + (as.slot * L::kR0 + (GI - g_lo)) * 8,
-                                  m.neg_zero_point(GI));
-                });
-                tmem_wait_st();
-                tc_fence_before();
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars.filled[as.slot]);
-        }
-        as.next();
-    };
     // Accumulators of one batch (scales from m) into acc.
     auto read_d = [&](auto bc, const RM& m) {
         constexpr int BB = decltype(bc)::value;
@@ -783,20 +809,11 @@ __device__ __forceinline__ void epilogue_warp(const Ctx& c, B& bars, uint32_t tm
     constexpr std::integral_constant<int, 0> kB0{};
     constexpr std::integral_constant<int, 1> kB1{};
     RM cur, nxt;
-    if (n_units > 0) {
-        fetch(cur);
-        write_z(kB0, cur);
-        write_z(kB1, cur);
-    }
+    if (n_units > 0) fetch(cur);
     bool seg_from_start = cc.i == 0;  // the open segment began at its tile's first k-stage
     for (int k = 0; k < n_units; ++k) {
-        const bool more = k + 1 < n_units;
-        if (more) fetch(nxt);
+        if (k + 1 < n_units) fetch(nxt);
         read_d(kB0, cur);
-        if (more) {
-            write_z(kB0, nxt);
-            write_z(kB1, nxt);
-        }
         read_d(kB1, cur);
         // a tile segment ends with the tile or with the CTA's share of the phase
         const bool tile_end = cc.i == cc.v.I - 1;
@@ -901,11 +918,11 @@ __global__ void __launch_bounds__(Lay<BITS, G>::kThreads, 1)
     const int lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            mbar_init(&bars.full[s], 1);
+            mbar_init(&bars.full[s], 1 + 32);  // TMA (expect_tx) + the producer warp's zero points
             mbar_init(&bars.empty[s], L::kUW + 1);
         }
         for (int s = 0; s < L::kNA; ++s) {
-            mbar_init(&bars.filled[s], L::kUW + (L::kZtc ? L::kEW : 0));
+            mbar_init(&bars.filled[s], L::kUW);
             mbar_init(&bars.afree[s], 1);
         }
         for (int s = 0; s < L::kND; ++s) {
@@ -934,15 +951,16 @@ __global__ void __launch_bounds__(Lay<BITS, G>::kThreads, 1)
 
     if (warp == L::kProducerWarp) {
         // ------------------------------------------------------------ producer
-        if (lane != 0) return;
+        // Lane 0 issues the TMA loads (and, in a fused step, holds back the X
+        // of a projection whose inputs are not complete yet); every lane then
+        // stages the zero points of four of the tile's rows into the stage and
+        // arrives on the stage's barrier once they have landed.
         const uint64_t pol_w = policy_evict_first();
         const uint64_t pol_x = policy_evict_last();
         Cursor cu;
         cu.init(c);
         int maps_of = -1;   // projection whose tensor maps were last prefetched
         int verified = -1;  // projections 0..verified of the launch known complete
-        // X loads held back until their projection's inputs are complete (fused
-        // step): the stage's packed words are loaded meanwhile.
         constexpr int kQ = 8;
         static_assert(S <= kQ, "pending queue holds a ring's worth of stages");
         uint32_t q_slot[kQ];
@@ -962,91 +980,127 @@ __global__ void __launch_bounds__(Lay<BITS, G>::kThreads, 1)
             }
         };
         auto pop_x = [&]() {
-            issue_x(q_slot[q_head], q_map[q_head], q_i[q_head], q_x3d[q_head]);
-            q_head = (q_head + 1) % kQ;
-            --q_n;
+            if constexpr (MULTI) {
+                issue_x(q_slot[q_head], q_map[q_head], q_i[q_head], q_x3d[q_head]);
+                q_head = (q_head + 1) % kQ;
+                --q_n;
+            }
         };
         Ring<S> st;
         uint32_t it = 0;
         bool ok = true;
         for (int k = 0; k < n_units; ++k, ++it) {
-            if (cu.p != maps_of) {
-                prefetch_tensormap(cu.v.tmW);
-                prefetch_tensormap(cu.v.tmX);
-                maps_of = cu.p;
-            }
-            if (k == 0 || cu.i == 0) {
-                // warm L2 with the tile's scales and zero points (whole rows, rounded inward)
-                const int r0 = cu.t * kBN, r1 = min(cu.v.N, r0 + kBN);
-                const uintptr_t sb = reinterpret_cast<uintptr_t>(cu.v.scales + static_cast<size_t>(r0) * cu.v.ng);
-                const uintptr_t se = reinterpret_cast<uintptr_t>(cu.v.scales + static_cast<size_t>(r1) * cu.v.ng);
-                const uintptr_t zb = reinterpret_cast<uintptr_t>(cu.v.zeros + static_cast<size_t>(r0) * cu.v.ng);
-                const uintptr_t ze = reinterpret_cast<uintptr_t>(cu.v.zeros + static_cast<size_t>(r1) * cu.v.ng);
-                const uintptr_t sb16 = (sb + 15) & ~uintptr_t(15), se16 = se & ~uintptr_t(15);
-                const uintptr_t zb16 = (zb + 15) & ~uintptr_t(15), ze16 = ze & ~uintptr_t(15);
-                if (se16 > sb16)
-                    prefetch_l2_bulk(reinterpret_cast<const void*>(sb16), static_cast<uint32_t>(se16 - sb16));
-                if (ze16 > zb16)
-                    prefetch_l2_bulk(reinterpret_cast<const void*>(zb16), static_cast<uint32_t>(ze16 - zb16));
-            }
-            if constexpr (MULTI) {
-                // a held-back stage occupying the slot needed now cannot drain without its X
-                while (ok && q_n > 0 && q_k[q_head] <= k - S) {
-                    if (!wait_deps(c, q_after[q_head], verified, abort_flag)) ok = false;
-                    else pop_x();
+            if (lane == 0) {
+                if (cu.p != maps_of) {
+                    prefetch_tensormap(cu.v.tmW);
+                    prefetch_tensormap(cu.v.tmX);
+                    maps_of = cu.p;
                 }
-                if (!ok) {
-                    record_error_tc(c.err, abort_flag);
-                    break;
+                if (k == 0 || cu.i == 0) {
+                    // warm L2 with the tile's scales (the epilogue reads them later)
+                    const int r0 = cu.t * kBN, r1 = min(cu.v.N, r0 + kBN);
+                    const uintptr_t sb = reinterpret_cast<uintptr_t>(cu.v.scales + static_cast<size_t>(r0) * cu.v.ng);
+                    const uintptr_t se = reinterpret_cast<uintptr_t>(cu.v.scales + static_cast<size_t>(r1) * cu.v.ng);
+                    const uintptr_t sb16 = (sb + 15) & ~uintptr_t(15), se16 = se & ~uintptr_t(15);
+                    if (se16 > sb16)
+                        prefetch_l2_bulk(reinterpret_cast<const void*>(sb16), static_cast<uint32_t>(se16 - sb16));
+                }
+                if constexpr (MULTI) {
+                    // a held-back stage occupying the slot needed now cannot drain without its X
+                    while (ok && q_n > 0 && q_k[q_head] <= k - S) {
+                        if (!wait_deps(c, q_after[q_head], verified, abort_flag)) ok = false;
+                        else pop_x();
+                    }
+                }
+                if (ok && !mbar_wait(&bars.empty[st.slot], st.phase ^ 1u, abort_flag)) ok = false;
+                if (ok) {
+                    uint8_t* stage = smem + st.slot * L::kStageBytes;
+                    uint64_t* fb = &bars.full[st.slot];
+                    mbar_arrive_expect_tx(fb, L::kWBytes + L::kXBytes);
+#pragma unroll
+                    for (int b = 0; b < L::kBoxes; ++b)
+                        tma_load_2d(stage + b * L::kBoxBytes, cu.v.tmW,
+                                    (cu.i * L::kBoxes + b) * kWordsPerStage, cu.t * kBN, fb, pol_w);
+                    if (!MULTI || cu.v.after < 0 || (q_n == 0 && deps_ready(c, cu.v.after, verified))) {
+                        issue_x(st.slot, cu.v.tmX, cu.i, cu.v.x3d);
+                    } else {
+                        const int e = (q_head + q_n) % kQ;
+                        q_slot[e] = st.slot;
+                        q_map[e] = cu.v.tmX;
+                        q_i[e] = cu.i;
+                        q_x3d[e] = cu.v.x3d;
+                        q_after[e] = cu.v.after;
+                        q_k[e] = k;
+                        ++q_n;
+                    }
+                    if constexpr (MULTI)
+                        while (q_n > 0 && deps_ready(c, q_after[q_head], verified)) pop_x();
                 }
             }
-            if (!mbar_wait(&bars.empty[st.slot], st.phase ^ 1u, abort_flag)) {
-                record_error_tc(c.err, abort_flag);
-                ok = false;
+            ok = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;
+            if (!ok) {
+                if (lane == 0) record_error_tc(c.err, abort_flag);
                 break;
             }
-            uint8_t* stage = smem + st.slot * L::kStageBytes;
-            uint64_t* fb = &bars.full[st.slot];
-            mbar_arrive_expect_tx(fb, L::kWBytes + L::kXBytes);
+            // zero points of rows lane, lane + 32, lane + 64, lane + 96
+            {
+                const uint32_t zdst = smem_u32 + st.slot * L::kStageBytes + L::kZOff;
+                const long long g0 = static_cast<long long>(cu.i) * L::kGPS;
 #pragma unroll
-            for (int b = 0; b < L::kBoxes; ++b)
-                tma_load_2d(stage + b * L::kBoxBytes, cu.v.tmW, (cu.i * L::kBoxes + b) * kWordsPerStage,
-                            cu.t * kBN, fb, pol_w);
-            if (!MULTI || cu.v.after < 0 || (q_n == 0 && deps_ready(c, cu.v.after, verified))) {
-                issue_x(st.slot, cu.v.tmX, cu.i, cu.v.x3d);
-            } else {
-                const int e = (q_head + q_n) % kQ;
-                q_slot[e] = st.slot;
-                q_map[e] = cu.v.tmX;
-                q_i[e] = cu.i;
-                q_x3d[e] = cu.v.x3d;
-                q_after[e] = cu.v.after;
-                q_k[e] = k;
-                ++q_n;
+                for (int j = 0; j < 4; ++j) {
+                    const int row = lane + 32 * j;
+                    const int n = cu.t * kBN + row;
+                    const bool in = n < cu.v.N;
+                    const uint32_t dst = zdst + row * L::kZRow;
+                    if constexpr (L::kZAsync) {
+                        if (cu.v.meta_vec) {
+                            const uint8_t* src = cu.v.zeros + (in ? static_cast<size_t>(n) * cu.v.ng + g0 : 0);
+                            cp_async_n<L::kZRow>(dst, src, in ? L::kZRow : 0);
+                            continue;
+                        }
+                    }
+                    uint32_t zw[L::kZRow / 4];
+#pragma unroll
+                    for (int w = 0; w < L::kZRow / 4; ++w) zw[w] = 0;
+                    if (in) {
+                        const uint8_t* src = cu.v.zeros + static_cast<size_t>(n) * cu.v.ng + g0;
+                        for (int gi = 0; gi < L::kGPS; ++gi)
+                            if (g0 + gi < cu.v.ng)
+                                zw[gi / 4] |= static_cast<uint32_t>(__ldg(src + gi)) << (8 * (gi & 3));
+                    }
+#pragma unroll
+                    for (int w = 0; w < L::kZRow / 4; ++w) sts32(dst + 4 * w, zw[w]);
+                }
+                // one arrival per lane: after its copies land, or (plain stores)
+                // a release arrive
+                if (L::kZAsync && cu.v.meta_vec)
+                    cp_async_arrive(&bars.full[st.slot]);
+                else
+                    mbar_arrive(&bars.full[st.slot]);
             }
-            if constexpr (MULTI)
-                while (q_n > 0 && deps_ready(c, q_after[q_head], verified)) pop_x();
             cu.next(c);
             st.next();
         }
-        if constexpr (MULTI) {
-            while (ok && q_n > 0) {
-                if (!wait_deps(c, q_after[q_head], verified, abort_flag)) {
-                    record_error_tc(c.err, abort_flag);
-                    ok = false;
-                } else {
-                    pop_x();
+        if (lane == 0) {
+            if constexpr (MULTI) {
+                while (ok && q_n > 0) {
+                    if (!wait_deps(c, q_after[q_head], verified, abort_flag)) {
+                        record_error_tc(c.err, abort_flag);
+                        ok = false;
+                    } else {
+                        pop_x();
+                    }
                 }
+                // on failure: issue what was held back (the results are discarded)
+                // so that every stage in flight completes before shared memory goes away
+                while (q_n > 0) pop_x();
             }
-            // on failure: issue what was held back (the results are discarded)
-            // so that every stage in flight completes before shared memory goes away
-            while (q_n > 0) pop_x();
-        }
-        if (!ok) {
-            // let copies already in flight land before the CTA's shared memory goes away
-            const uint32_t first = it > S ? it - S : 0;
-            volatile int never = 0;
-            for (uint32_t j = first; j < it; ++j) mbar_wait(&bars.full[j % S], (j / S) & 1u, &never);
+            if (!ok) {
+                // let copies already in flight land before the CTA's shared memory goes away
+                const uint32_t first = it > S ? it - S : 0;
+                volatile int never = 0;
+                for (uint32_t j = first; j < it; ++j) mbar_wait(&bars.full[j % S], (j / S) & 1u, &never);
+            }
         }
         return;
     }

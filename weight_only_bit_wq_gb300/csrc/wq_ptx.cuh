@@ -184,6 +184,24 @@ __device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, uint32_
                  : "memory");
 }
 
+// 4/8/16-byte asynchronous global -> shared copy (src and dst aligned to the
+// size); with src_bytes = 0 the destination is zero-filled and src is not read.
+template <int BYTES>
+__device__ __forceinline__ void cp_async_n(uint32_t dst, const void* src, uint32_t src_bytes) {
+    static_assert(BYTES == 4 || BYTES == 8 || BYTES == 16, "cp.async size");
+    asm volatile("cp.async.ca.shared.global [%0], [%1], %2, %3;" ::"r"(dst), "l"(src), "n"(BYTES),
+                 "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+// Wait until at most N of this thread's committed cp.async groups are pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // Arrive on `bar` once every cp.async issued so far by this thread has landed.
 __device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
     asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar))
@@ -213,6 +231,10 @@ __device__ __forceinline__ int ld_acquire_gpu(const int* p) {
 // acquired) before its later async-proxy (TMA) accesses.
 __device__ __forceinline__ void fence_proxy_async() {
     asm volatile("fence.proxy.async;" ::: "memory");
+}
+
+__device__ __forceinline__ void sts32(uint32_t addr, uint32_t v) {
+    asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 
 __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
