@@ -640,7 +640,8 @@ __device__ __forceinline__ void finish_rows(const Ctx& c, const ProjView& v, int
 // Shared-memory barriers of one CTA.
 template <int S, int NA, int ND>
 struct Bars {
-    uint64_t full[S];    // stage landed (TMA transaction bytes)
+    uint64_t full[S];    // stage's packed words and zero points landed (TMA bytes + producer lanes)
+    uint64_t xfull[S];   // stage's X slice landed (TMA bytes)
     uint64_t empty[S];   // stage consumed: unpack warps + one MMA commit
     uint64_t filled[NA]; // A slot written (unpack warps)
     uint64_t afree[NA];  // A slot's MMAs complete (tcgen05.commit)
@@ -919,6 +920,7 @@ __global__ void __launch_bounds__(Lay<BITS, G>::kThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(&bars.full[s], 1 + 32);  // TMA (expect_tx) + the producer warp's zero points
+            mbar_init(&bars.xfull[s], 1);
             mbar_init(&bars.empty[s], L::kUW + 1);
         }
         for (int s = 0; s < L::kNA; ++s) {
@@ -970,13 +972,15 @@ __global__ void __launch_bounds__(Lay<BITS, G>::kThreads, 1)
         int q_head = 0, q_n = 0;
         auto issue_x = [&](uint32_t slot, const CUtensorMap* map, int i, bool x3d) {
             uint8_t* stage = smem + slot * L::kStageBytes;
+            uint64_t* xb = &bars.xfull[slot];
+            mbar_arrive_expect_tx(xb, L::kXBytes);
             if (x3d) {
-                tma_load_3d(stage + L::kWBytes, map, 0, 0, i * L::kXBoxes, &bars.full[slot], pol_x);
+                tma_load_3d(stage + L::kWBytes, map, 0, 0, i * L::kXBoxes, xb, pol_x);
             } else {
 #pragma unroll
                 for (int b = 0; b < L::kXBoxes; ++b)
                     tma_load_2d(stage + L::kWBytes + b * L::kXBoxBytes, map,
-                                i * L::kStageValues + b * L::kXBoxValues, 0, &bars.full[slot], pol_x);
+                                i * L::kStageValues + b * L::kXBoxValues, 0, xb, pol_x);
             }
         };
         auto pop_x = [&]() {
@@ -1016,7 +1020,7 @@ __global__ void __launch_bounds__(Lay<BITS, G>::kThreads, 1)
                 if (ok) {
                     uint8_t* stage = smem + st.slot * L::kStageBytes;
                     uint64_t* fb = &bars.full[st.slot];
-                    mbar_arrive_expect_tx(fb, L::kWBytes + L::kXBytes);
+                    mbar_arrive_expect_tx(fb, L::kWBytes);
 #pragma unroll
                     for (int b = 0; b < L::kBoxes; ++b)
                         tma_load_2d(stage + b * L::kBoxBytes, cu.v.tmW,
@@ -1099,7 +1103,10 @@ __global__ void __launch_bounds__(Lay<BITS, G>::kThreads, 1)
                 // let copies already in flight land before the CTA's shared memory goes away
                 const uint32_t first = it > S ? it - S : 0;
                 volatile int never = 0;
-                for (uint32_t j = first; j < it; ++j) mbar_wait(&bars.full[j % S], (j / S) & 1u, &never);
+                for (uint32_t j = first; j < it; ++j) {
+                    mbar_wait(&bars.full[j % S], (j / S) & 1u, &never);
+                    mbar_wait(&bars.xfull[j % S], (j / S) & 1u, &never);
+                }
             }
         }
         return;
@@ -1114,7 +1121,8 @@ __global__ void __launch_bounds__(Lay<BITS, G>::kThreads, 1)
         Ring<L::kNA> as;
         Ring<L::kND> ds;
         for (int k = 0; k < n_units && ok; ++k) {
-            if (!wait_all(&bars.full[st.slot], st.phase, abort_flag)) {
+            // the MMAs read only the stage's X (A comes from tensor memory)
+            if (!wait_all(&bars.xfull[st.slot], st.phase, abort_flag)) {
                 ok = false;
                 break;
             }
