@@ -155,7 +155,9 @@ wq_status_t wq_gemm_noalloc(const uint16_t* x, const uint32_t* wq, const uint16_
  * Read back the kernel error word of a workspace (NULL = the library buffer
  * of the current device) after synchronising `stream`: WQ_OK, or
  * WQ_ERR_TIMEOUT if a kernel abandoned a bounded wait since the last check.
- * Clears the word.
+ * Clears the word.  After WQ_ERR_TIMEOUT the library buffer has been zeroed
+ * whole; a caller-owned workspace may still hold split-K counters of the
+ * abandoned launch and must be zeroed again (wq_workspace_init) before reuse.
  */
 wq_status_t wq_check_workspace(void* workspace, void* stream);
 

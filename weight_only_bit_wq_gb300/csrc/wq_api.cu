@@ -369,8 +369,17 @@ wq_status_t wq_check_workspace(void* workspace, void* stream) {
     int word = 0;
     if ((e = cudaMemcpy(&word, ws, sizeof word, cudaMemcpyDeviceToHost)) != cudaSuccess) return cuda_fail(e);
     if (word == 0) return WQ_OK;
-    const int zero = 0;
-    if ((e = cudaMemcpy(ws, &zero, sizeof zero, cudaMemcpyHostToDevice)) != cudaSuccess) return cuda_fail(e);
+    // A launch that gave up may have left split-K counters behind: the
+    // library buffer is zeroed whole; a caller's workspace gets its error
+    // word cleared and must be zeroed again (wq_workspace_init) before reuse.
+    DeviceInfo* d = nullptr;
+    if (!workspace && device_info(&d) == WQ_OK && d->lib_ws == ws) {
+        if ((e = cudaMemset(ws, 0, d->lib_ws_bytes)) != cudaSuccess) return cuda_fail(e);
+    } else {
+        const int zero = 0;
+        if ((e = cudaMemcpy(ws, &zero, sizeof zero, cudaMemcpyHostToDevice)) != cudaSuccess)
+            return cuda_fail(e);
+    }
     return WQ_ERR_TIMEOUT;
 }
 
