@@ -183,7 +183,13 @@ typedef struct wq_proj_desc {
 } wq_proj_desc_t;
 
 /* Step modes.
- * 0 (sequential): one wq_gemm launch per projection, in order.
+ * 0 (sequential): one wq_gemm launch per projection, in order.  Each launch
+ *   that directly follows another of the step is a programmatic dependent
+ *   launch: its CTAs start as the previous kernel's leave and load their
+ *   first packed weights, zero points and scales at once, while x and y are
+ *   touched only after the previous kernel has completed.  So the packed
+ *   weights, scales and zero points of a step must not be written by the
+ *   step itself (x may be: it is produced by the previous projection).
  * WQ_STEP_FUSED: one persistent launch per run of consecutive projections
  *   with the same bit width and group size.  The launch streams the units of
  *   all its projections back to back (stream-K across projection

@@ -297,15 +297,15 @@ wq_status_t host_encode_proj(const uint16_t* x, const uint32_t* wq, const uint16
 
 }  // namespace wq
 
-extern "C" {
+namespace wq {
 
-wq_status_t wq_gemm(const uint16_t* x, const uint32_t* wq, const uint16_t* scales,
-                    const uint8_t* zeros, float* y, int M, int N, int K, int group, int bits,
-                    void* workspace, size_t workspace_bytes, void* stream) {
-    if (wq_status_t st = wq::host_check_gemm(x, wq, scales, zeros, y, M, N, K, group, bits))
+wq_status_t gemm_run(const uint16_t* x, const uint32_t* wq, const uint16_t* scales,
+                     const uint8_t* zeros, float* y, int M, int N, int K, int group, int bits,
+                     void* workspace, size_t workspace_bytes, cudaStream_t s, bool pdl) {
+    if (wq_status_t st = host_check_gemm(x, wq, scales, zeros, y, M, N, K, group, bits))
         return st;
     if (M == 0 || N == 0) return WQ_OK;
-    cudaStream_t s = as_stream(stream);
+
     if (K == 0) {  // empty sum
         cudaError_t e = cudaMemsetAsync(y, 0, static_cast<size_t>(M) * N * sizeof(float), s);
         return e == cudaSuccess ? WQ_OK : cuda_fail(e);
@@ -344,6 +344,7 @@ wq_status_t wq_gemm(const uint16_t* x, const uint32_t* wq, const uint16_t* scale
     a.I = I;
     a.U = static_cast<long long>(T) * I;
     a.P = wq::choose_grid(T, I, d->sm_count);
+    a.pdl = pdl ? 1 : 0;
 
     cudaError_t e;
     if (bits == 4)
@@ -356,6 +357,16 @@ wq_status_t wq_gemm(const uint16_t* x, const uint32_t* wq, const uint16_t* scale
     return e == cudaSuccess ? WQ_OK : cuda_fail(e);
 }
 
+}  // namespace wq
+
+extern "C" {
+
+wq_status_t wq_gemm(const uint16_t* x, const uint32_t* wq, const uint16_t* scales,
+                    const uint8_t* zeros, float* y, int M, int N, int K, int group, int bits,
+                    void* workspace, size_t workspace_bytes, void* stream) {
+    return wq::gemm_run(x, wq, scales, zeros, y, M, N, K, group, bits, workspace, workspace_bytes,
+                        as_stream(stream), false);
+}
 wq_status_t wq_check_workspace(void* workspace, void* stream) {
     void* ws = workspace;
     if (!ws) {

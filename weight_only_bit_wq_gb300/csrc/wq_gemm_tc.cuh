@@ -933,6 +933,8 @@ __global__ void __launch_bounds__(Lay<BITS, G>::kThreads, 1)
         }
         mbar_init(&bars.drain, 1);
         *abort_flag = 0;
+        // a dependent launch may place its CTAs on SMs as this grid's CTAs leave
+        griddep_launch_dependents();
         long long n = 0;
         for (int ph = 0; ph < c.nphase; ++ph)
             n += c.sub_lo(ph, blockIdx.x + 1) - c.sub_lo(ph, blockIdx.x);
@@ -990,6 +992,14 @@ __global__ void __launch_bounds__(Lay<BITS, G>::kThreads, 1)
                 --q_n;
             }
         };
+        // A dependent launch (single projection) streams the packed words and
+        // zero points of its first stages at once; their X (and everything
+        // after) waits until the previous kernel has completed.  Two stages
+        // measured best: a longer hold releases a burst of X loads late.
+        constexpr int kHeld = S < 2 ? S : 2;
+        const bool hold_x = !MULTI && a.pdl != 0;
+        const int n_held = hold_x ? (n_units < kHeld ? n_units : kHeld) : 0;
+        const int u_first = static_cast<int>(c.sub_lo(0, blockIdx.x));
         Ring<S> st;
         uint32_t it = 0;
         bool ok = true;
@@ -1025,7 +1035,15 @@ __global__ void __launch_bounds__(Lay<BITS, G>::kThreads, 1)
                     for (int b = 0; b < L::kBoxes; ++b)
                         tma_load_2d(stage + b * L::kBoxBytes, cu.v.tmW,
                                     (cu.i * L::kBoxes + b) * kWordsPerStage, cu.t * kBN, fb, pol_w);
-                    if (!MULTI || cu.v.after < 0 || (q_n == 0 && deps_ready(c, cu.v.after, verified))) {
+                    if (k < n_held) {
+                        if (k == n_held - 1) {
+                            // X of the held stages (slots 0.., units u_first..) once
+                            // the previous kernel has completed
+                            griddep_wait();
+                            for (int kk = 0; kk < n_held; ++kk)
+                                issue_x(static_cast<uint32_t>(kk), cu.v.tmX, (u_first + kk) % cu.v.I, cu.v.x3d);
+                        }
+                    } else if (!MULTI || cu.v.after < 0 || (q_n == 0 && deps_ready(c, cu.v.after, verified))) {
                         issue_x(st.slot, cu.v.tmX, cu.i, cu.v.x3d);
                     } else {
                         const int e = (q_head + q_n) % kQ;
@@ -1100,6 +1118,13 @@ __global__ void __launch_bounds__(Lay<BITS, G>::kThreads, 1)
                 while (q_n > 0) pop_x();
             }
             if (!ok) {
+                // stages whose X was still held back get it now (the previous
+                // kernel always completes), so that every stage in flight lands
+                if (hold_x && static_cast<int>(it) < n_held) {
+                    griddep_wait();
+                    for (int kk = 0; kk < static_cast<int>(it); ++kk)
+                        issue_x(static_cast<uint32_t>(kk), c.one.tmX, (u_first + kk) % c.one.I, c.one.x3d);
+                }
                 // let copies already in flight land before the CTA's shared memory goes away
                 const uint32_t first = it > S ? it - S : 0;
                 volatile int never = 0;
@@ -1199,8 +1224,21 @@ cudaError_t launch_tc(const CUtensorMap& tmW, const CUtensorMap& tmX, const Gemm
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
     if (e != cudaSuccess) return e;
-    kern<<<a.P, L::kThreads, L::kSmemBytes, s>>>(tmW, tmX, a, StepArgs{});
-    return cudaGetLastError();
+    if (!a.pdl) {
+        kern<<<a.P, L::kThreads, L::kSmemBytes, s>>>(tmW, tmX, a, StepArgs{});
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(a.P));
+    cfg.blockDim = dim3(L::kThreads);
+    cfg.dynamicSmemBytes = L::kSmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, tmW, tmX, a, StepArgs{});
 }
 
 // Fused step launch; cooperative (all CTAs resident at once) when projections

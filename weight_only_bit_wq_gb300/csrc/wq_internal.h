@@ -40,6 +40,8 @@ struct GemmArgs {
     int P;            // CTAs
     int meta_vec;     // scales/zeros 16-byte aligned and K/group a multiple of the groups per stage
     int x3d;          // X map is 3-D [K/64][M][64]: one TMA box per stage (K % 64 == 0)
+    int pdl;          // launched as a programmatic dependent of the previous kernel on the
+                      // stream: X is read, and anything written, once that kernel completed
 };
 
 // One projection of a fused step, as the step kernel reads it from device
@@ -100,6 +102,13 @@ cudaError_t launch_gemm_tc_b2(int group, const CUtensorMap& tmW, const CUtensorM
 cudaError_t launch_step_b4(int group, const StepArgs& sa, bool cooperative, cudaStream_t s);
 cudaError_t launch_step_b3(int group, const StepArgs& sa, bool cooperative, cudaStream_t s);
 cudaError_t launch_step_b2(int group, const StepArgs& sa, bool cooperative, cudaStream_t s);
+
+// wq_gemm with the launch mode chosen by the caller: pdl = launch as a
+// programmatic dependent of the previous kernel on the stream (only where
+// that kernel writes none of wq, scales and zeros).
+wq_status_t gemm_run(const uint16_t* x, const uint32_t* wq, const uint16_t* scales,
+                     const uint8_t* zeros, float* y, int M, int N, int K, int group, int bits,
+                     void* workspace, size_t workspace_bytes, cudaStream_t s, bool pdl);
 
 // Host helpers shared by the entry points (wq_api.cu).
 wq_status_t host_cuda_fail(cudaError_t e);

@@ -227,6 +227,16 @@ __device__ __forceinline__ int ld_acquire_gpu(const int* p) {
     return v;
 }
 
+// Programmatic dependent launch: let the next kernel on the stream place its
+// CTAs as this grid's CTAs leave, and wait (in a dependent kernel) until the
+// previous kernel has completed and its writes are visible.
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // Orders this thread's earlier generic-proxy accesses (and what they
 // acquired) before its later async-proxy (TMA) accesses.
 __device__ __forceinline__ void fence_proxy_async() {

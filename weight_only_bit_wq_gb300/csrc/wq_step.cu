@@ -179,9 +179,26 @@ wq_status_t launch_run(const Run& r, Tables tab, int nphase, long long units, bo
 }
 
 wq_status_t run_single(const wq_proj_desc_t& p, void* workspace, size_t workspace_bytes,
-                       cudaStream_t s) {
-    return wq_gemm(p.x, p.wq, p.scales, p.zeros, p.y, p.M, p.N, p.K, p.group, p.bits, workspace,
-                   workspace_bytes, s);
+                       cudaStream_t s, bool pdl = false) {
+    return wq::gemm_run(p.x, p.wq, p.scales, p.zeros, p.y, p.M, p.N, p.K, p.group, p.bits,
+                        workspace, workspace_bytes, s, pdl);
+}
+
+bool launches_kernel(const wq_proj_desc_t& p) { return p.M > 0 && p.N > 0 && p.K > 0; }
+
+// Sequential mode: one wq_gemm per projection.  Every GEMM that directly
+// follows another is a programmatic dependent launch: its CTAs start as the
+// previous kernel's leave and stream their first packed words at once, and
+// X is read only after the previous kernel has completed (no GEMM of a step
+// writes packed words, scales or zero points).
+wq_status_t run_sequential(const wq_proj_desc_t* projs, int count, void* workspace,
+                           size_t workspace_bytes, cudaStream_t s) {
+    bool prev_gemm = false;
+    for (int i = 0; i < count; ++i) {
+        if (wq_status_t st = run_single(projs[i], workspace, workspace_bytes, s, prev_gemm)) return st;
+        prev_gemm = launches_kernel(projs[i]);
+    }
+    return WQ_OK;
 }
 
 // Upload every run's tables to `base` (table_bytes(count) of device memory),
@@ -277,9 +294,7 @@ wq_status_t wq_step_run_ex(const wq_proj_desc_t* projs, int count, unsigned flag
     if (flags & ~WQ_STEP_FUSED) return WQ_ERR_INVALID_ARG;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (flags & WQ_STEP_FUSED) return run_fused(projs, count, workspace, workspace_bytes, s, nullptr);
-    for (int i = 0; i < count; ++i)
-        if (wq_status_t st = run_single(projs[i], workspace, workspace_bytes, s)) return st;
-    return WQ_OK;
+    return run_sequential(projs, count, workspace, workspace_bytes, s);
 }
 
 wq_status_t wq_step_run(const wq_proj_desc_t* projs, int count, void* workspace,
@@ -316,9 +331,7 @@ wq_status_t wq_step_graph_create_ex(const wq_proj_desc_t* projs, int count, unsi
         if (flags & WQ_STEP_FUSED) {
             run = run_fused(projs, count, workspace, workspace_bytes, s, g->tables);
         } else {
-            run = WQ_OK;
-            for (int i = 0; i < count && run == WQ_OK; ++i)
-                run = run_single(projs[i], workspace, workspace_bytes, s);
+            run = run_sequential(projs, count, workspace, workspace_bytes, s);
         }
         cudaError_t e = cudaStreamEndCapture(s, &g->graph);
         if (run != WQ_OK) st = run;
