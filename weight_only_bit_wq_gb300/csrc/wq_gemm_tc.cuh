@@ -569,9 +569,14 @@ struct Cursor {
 // (tile, lane quarter) pair has its own arrival counter, so warps never wait
 // for one another.  In a fused step the warp that writes the final Y rows
 // then counts them done for the projection.
+//   likely_last: the segment holds the tile's first units and ends the CTA's
+//   share; the tile's other contributors took its later units at the start
+//   of their shares, so they have usually all arrived already.  Then the
+//   warp checks the counter first and, if they have, sums at once without
+//   publishing its own partial (two round trips fewer at the end of a share).
 __device__ __forceinline__ void finish_rows(const Ctx& c, const ProjView& v, int p,
-                                            const float (&acc)[kN], int t, bool whole, int r,
-                                            int q, int lane) {
+                                            const float (&acc)[kN], int t, bool whole,
+                                            bool likely_last, int r, int q, int lane) {
     const int n = t * kBN + r;
     const int gt = v.toff + t;
     auto count_done = [&]() {
@@ -592,29 +597,38 @@ __device__ __forceinline__ void finish_rows(const Ctx& c, const ProjView& v, int
     // slot 1 that of the tile it ends in (a share that started before this
     // tile's first unit ends in it).
     const long long tu0 = v.uoff + static_cast<long long>(t) * v.I;
-    const int own_role = c.sub_lo(v.phase, blockIdx.x) < tu0 ? 1 : 0;
-    float* mine = c.partials + static_cast<size_t>(2 * blockIdx.x + own_role) * (kMaxCols * kBN);
-#pragma unroll
-    for (int j = 0; j < kN; ++j)
-        if (j < v.M) __stcg(mine + j * kBN + r, acc[j]);
-    // The warp barrier orders every lane's partial before lane 0's release
-    // (acq_rel) increment; the reading warp's lane 0 acquires it and the next
-    // warp barrier orders the other lanes' reads after that acquire.
-    __syncwarp();
     const int b_first = c.owner(tu0, v.phase);
     const int b_last = c.owner(tu0 + v.I - 1, v.phase);
+    const int me = static_cast<int>(blockIdx.x);
     int* ctr = c.counters + static_cast<size_t>(gt) * kCountersPerTile + q;
-    int last = 0;
-    if (lane == 0) last = (atomic_add_acq_rel_gpu(ctr, 1) == b_last - b_first) ? 1 : 0;
-    last = __shfl_sync(kFull, last, 0);
-    if (!last) return;
     // contributors after the first start their share inside this tile (slot 0)
     const int first_role = c.sub_lo(v.phase, b_first) < tu0 ? 1 : 0;
+    int last = 0;
+    if (likely_last) {
+        int cnt = 0;
+        if (lane == 0) cnt = ld_acquire_gpu(ctr);
+        last = __shfl_sync(kFull, cnt, 0) == b_last - b_first ? 1 : 0;  // all others arrived
+    }
+    if (!last) {
+        const int own_role = c.sub_lo(v.phase, blockIdx.x) < tu0 ? 1 : 0;
+        float* mine = c.partials + static_cast<size_t>(2 * blockIdx.x + own_role) * (kMaxCols * kBN);
+#pragma unroll
+        for (int j = 0; j < kN; ++j)
+            if (j < v.M) __stcg(mine + j * kBN + r, acc[j]);
+        // The warp barrier orders every lane's partial before lane 0's release
+        // (acq_rel) increment; the reading warp's lane 0 acquires it and the
+        // next warp barrier orders the other lanes' reads after that acquire.
+        __syncwarp();
+        if (lane == 0) last = (atomic_add_acq_rel_gpu(ctr, 1) == b_last - b_first) ? 1 : 0;
+        if (!__shfl_sync(kFull, last, 0)) return;
+    }
+    __syncwarp();  // the other lanes' reads follow lane 0's acquire
+    // all contributors in k order (this warp's own sums in place of its partial)
     float tot[kN];
 #pragma unroll
     for (int j = 0; j < kN; ++j) tot[j] = 0.f;
     for (int b = b_first; b <= b_last; ++b) {
-        if (b == static_cast<int>(blockIdx.x)) {
+        if (b == me) {
 #pragma unroll
             for (int j = 0; j < kN; ++j) tot[j] += acc[j];
         } else {
@@ -820,7 +834,9 @@ __device__ __forceinline__ void epilogue_warp(const Ctx& c, B& bars, uint32_t tm
         const bool tile_end = cc.i == cc.v.I - 1;
         const bool end = tile_end || cc.last_of_share();
         if (end) {
-            if (!dead) finish_rows(c, cc.v, cc.p, acc, cc.t, seg_from_start && tile_end, r, q, lane);
+            if (!dead)
+                finish_rows(c, cc.v, cc.p, acc, cc.t, seg_from_start && tile_end,
+                            seg_from_start && !tile_end, r, q, lane);
 #pragma unroll
             for (int j = 0; j < kN; ++j) acc[j] = 0.f;
         }
