@@ -568,13 +568,13 @@ struct Cursor {
 // warp of the last CTA to finish the tile add all partials in k order.  Each
 // (tile, lane quarter) pair has its own arrival counter, so warps never wait
 // for one another.  In a fused step the warp that writes the final Y rows
-// then counts them done for the projection.
+// then counts them done for the projection's phase.
 //   likely_last: the segment holds the tile's first units and ends the CTA's
 //   share; the tile's other contributors took its later units at the start
 //   of their shares, so they have usually all arrived already.  Then the
 //   warp checks the counter first and, if they have, sums at once without
 //   publishing its own partial (two round trips fewer at the end of a share).
-__device__ __forceinline__ void finish_rows(const Ctx& c, const ProjView& v, int p,
+__device__ __forceinline__ void finish_rows(const Ctx& c, const ProjView& v,
                                             const float (&acc)[kN], int t, bool whole,
                                             bool likely_last, int r, int q, int lane) {
     const int n = t * kBN + r;
@@ -582,7 +582,7 @@ __device__ __forceinline__ void finish_rows(const Ctx& c, const ProjView& v, int
     auto count_done = [&]() {
         if (c.proj != nullptr) {
             __syncwarp();
-            if (lane == 0) red_add_release_gpu(c.done + p, 1);
+            if (lane == 0) red_add_release_gpu(c.done + v.phase, 1);
         }
     };
     if (whole) {
@@ -835,7 +835,7 @@ __device__ __forceinline__ void epilogue_warp(const Ctx& c, B& bars, uint32_t tm
         const bool end = tile_end || cc.last_of_share();
         if (end) {
             if (!dead)
-                finish_rows(c, cc.v, cc.p, acc, cc.t, seg_from_start && tile_end,
+                finish_rows(c, cc.v, acc, cc.t, seg_from_start && tile_end,
                             seg_from_start && !tile_end, r, q, lane);
 #pragma unroll
             for (int j = 0; j < kN; ++j) acc[j] = 0.f;
@@ -847,19 +847,17 @@ __device__ __forceinline__ void epilogue_warp(const Ctx& c, B& bars, uint32_t tm
     tc_fence_before();
 }
 
-// Producer's dependency check (fused step): true once projections 0..upto of
-// the launch are complete; `verified` caches how far that is known.
+// Producer's dependency check (fused step): true once phase `upto` of the
+// launch is complete (one counter per phase; a phase completes only after
+// every earlier one, whose results its X waited for); `verified` caches the
+// latest phase known complete.
 __device__ __forceinline__ bool deps_ready(const Ctx& c, int upto, int& verified) {
-    bool acquired = false;
-    while (verified < upto) {
-        const int j = verified + 1;
-        if (ld_acquire_gpu(c.done + j) < 4 * c.proj[j].T) break;  // 4 lane quarters per tile
-        verified = j;
-        acquired = true;
-    }
+    if (verified >= upto) return true;
+    if (ld_acquire_gpu(c.done + upto) < __ldg(&c.phase[upto].need)) return false;
+    verified = upto;
     // the TMA reads that follow are async-proxy accesses of data the acquire made visible
-    if (acquired) fence_proxy_async();
-    return verified >= upto;
+    fence_proxy_async();
+    return true;
 }
 
 // The same, waiting (bounded) until it holds.  Each poll is an L2 round

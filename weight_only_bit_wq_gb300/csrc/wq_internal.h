@@ -57,7 +57,7 @@ struct ProjDev {  // aligned like its tensor maps
     int M, N, ng, T, I;
     int toff;                // first global tile
     int meta_vec, x3d;
-    int after;               // X is read once projections 0..after of this launch are complete (-1: at once)
+    int after;               // X is read once phase `after` of this launch is complete (-1: at once)
     int phase;               // phase of the launch this projection belongs to
     int pad[4];
 };
@@ -68,6 +68,8 @@ struct ProjDev {  // aligned like its tensor maps
 struct PhaseDev {
     long long uoff;  // first global unit
     long long U;     // units of the phase
+    int need;        // finished (tile, lane quarter) pairs of a complete phase: 4 x its tiles
+    int pad;
 };
 static_assert(sizeof(ProjDev) % 64 == 0, "ProjDev keeps 64-byte alignment in arrays");
 
@@ -78,7 +80,7 @@ struct StepArgs {
     int nproj, nphase;
     float* partials;      // [2 * P][kMaxCols][kBN]
     int* counters;        // [total tiles][kCountersPerTile]
-    int* done;            // [nproj] finished (tile, lane quarter) pairs, zero at launch
+    int* done;            // [nphase] finished (tile, lane quarter) pairs per phase, zero at launch
     int* err;
     long long U;          // total units
     int P;

@@ -128,7 +128,7 @@ wq_status_t build_table(const wq_proj_desc_t* projs, const Run& r, std::vector<w
         if (li == 0 || after >= phase_start) {
             if (li > 0) *waits = true;
             phase_start = li;
-            phases.push_back({uoff, 0});
+            phases.push_back({uoff, 0, 0, 0});
         }
         d.scales = p.scales;
         d.zeros = p.zeros;
@@ -141,9 +141,12 @@ wq_status_t build_table(const wq_proj_desc_t* projs, const Run& r, std::vector<w
         d.uoff = uoff;
         d.toff = toff;
         d.phase = static_cast<int>(phases.size()) - 1;
-        d.after = phase_start > 0 ? phase_start - 1 : -1;
+        // a later phase waits for the one before it (which completes only after
+        // every earlier one: its X waited for them)
+        d.after = phase_start > 0 ? static_cast<int>(phases.size()) - 2 : -1;
         const long long u = static_cast<long long>(d.T) * d.I;
         phases.back().U += u;
+        phases.back().need += 4 * d.T;  // 4 lane quarters per tile
         uoff += u;
         toff += d.T;
     }
