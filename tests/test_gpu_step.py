@@ -179,3 +179,53 @@ def test_fused_step_bad_dependency_rejected():
     assert wq.wq_step_workspace_bytes(descs, wq.WQ_STEP_FUSED) == 0
     with pytest.raises(wq.WQError):
         wq.wq_step_run(descs, wq.new_workspace(1, 640, 640, 128, 4), flags=wq.WQ_STEP_FUSED)
+
+
+def test_sequential_step_with_empty_projections_between_gemms():
+    # Sequential mode launches a GEMM that follows another as a programmatic
+    # dependent; a projection with K = 0 (Y zero-filled, no kernel) or M = 0
+    # (nothing at all) between two GEMMs must break that chain cleanly.
+    import weight_only_bit_wq_gb300 as wq
+    shapes = [(640, 512, 4, 128), (640, 640, 2, 64), (1280, 640, 4, 64), (896, 1536, 3, 128)]
+    projs = []
+    for i, (K, N, bits, G) in enumerate(shapes):
+        p = synth.Projection(f"e{i}", 5, N, K, bits, G, 500, index=i)
+        w, x, d = to_dev_host_inputs(p)
+        d["y"] = torch.full((p.M, p.N), float("nan"), dtype=torch.float32, device=dev())
+        projs.append((p, w, x, d))
+    ref = [wq.wq_gemm(d["x"], d["wq"], d["s"], d["z"], p.N, p.group, p.bits).cpu().numpy()
+           for p, w, x, d in projs]
+    p0, _, _, d0 = projs[0]
+    y_k0 = torch.full((3, 700), float("nan"), dtype=torch.float32, device=dev())
+    y_m0 = torch.full((1, 1), float("nan"), dtype=torch.float32, device=dev())
+    entries = [dict(x=d["x"], wq=d["wq"], scales=d["s"], zeros=d["z"], y=d["y"], M=p.M, N=p.N,
+                    K=p.K, group=p.group, bits=p.bits) for p, w, x, d in projs]
+    k0 = dict(x=d0["x"], wq=d0["wq"], scales=d0["s"], zeros=d0["z"], y=y_k0, M=3, N=700, K=0,
+              group=128, bits=4)
+    m0 = dict(x=d0["x"], wq=d0["wq"], scales=d0["s"], zeros=d0["z"], y=y_m0, M=0, N=1, K=128,
+              group=128, bits=4)
+    order = [entries[0], entries[1], k0, entries[2], m0, entries[3]]
+    descs = wq.make_descs(order)
+    ws = wq.new_workspace(16, 1536, 1280, 32, 2)
+    for graph in (False, True):
+        for p, w, x, d in projs:
+            d["y"].fill_(float("nan"))
+        y_k0.fill_(float("nan"))
+        if graph:
+            stream = torch.cuda.Stream()
+            stream.wait_stream(torch.cuda.current_stream())
+            g = wq.StepGraph(descs, ws, stream=stream)
+            g.launch(stream=stream)
+            stream.synchronize()
+            g.close()
+        else:
+            wq.wq_step_run(descs, ws)
+            torch.cuda.synchronize()
+        for (p, w, x, d), r in zip(projs, ref):
+            assert (d["y"].cpu().numpy().view(np.uint32) == r.view(np.uint32)).all(), (p.name, graph)
+        assert (y_k0.cpu().numpy() == 0).all()
+        assert np.isnan(y_m0.cpu().numpy()).all()
+    wq.wq_check_workspace(ws)
+    p, w, x, d = projs[3]
+    err = rel_err(d["y"].cpu().numpy(), oracle_gemm(p, w, x))
+    assert err <= REL_TOL and err <= ARITH_TOL

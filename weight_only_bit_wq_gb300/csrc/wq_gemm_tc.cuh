@@ -981,10 +981,10 @@ __global__ void __launch_bounds__(Lay<BITS, G>::kThreads, 1)
         int verified = -1;  // projections 0..verified of the launch known complete
         constexpr int kQ = 8;
         static_assert(S <= kQ, "pending queue holds a ring's worth of stages");
-        uint32_t q_slot[kQ];
-        const CUtensorMap* q_map[kQ];
-        int q_i[kQ], q_after[kQ], q_k[kQ];
-        bool q_x3d[kQ];
+        uint32_t q_slot[kQ] = {};
+        const CUtensorMap* q_map[kQ] = {};
+        int q_i[kQ] = {}, q_after[kQ] = {}, q_k[kQ] = {};
+        bool q_x3d[kQ] = {};
         int q_head = 0, q_n = 0;
         auto issue_x = [&](uint32_t slot, const CUtensorMap* map, int i, bool x3d) {
             uint8_t* stage = smem + slot * L::kStageBytes;
