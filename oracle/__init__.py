@@ -48,6 +48,9 @@ def _load() -> ctypes.CDLL:
         lib.wqo_bf16_rne.argtypes = [ctypes.c_double]
         lib.wqo_bf16_rne.restype = ctypes.c_uint16
         lib.wqo_gemm_f64.argtypes = [P, P, P, P, P, i, i, i, i, i, i]
+        lib.wqo_silu_f64.argtypes = [ctypes.c_double]
+        lib.wqo_silu_f64.restype = ctypes.c_double
+        lib.wqo_swiglu_bf16.argtypes = [P, i, i, P]
         lib.wqo_max_threads.argtypes = [i]
         for fn in (lib.wqo_pack, lib.wqo_unpack, lib.wqo_dequant_f64, lib.wqo_dequant_bf16,
                    lib.wqo_gemm_f64, lib.wqo_max_threads):
@@ -121,6 +124,22 @@ def gemm_f64(x, wq, s, z, K: int, group: int, bits: int, threads: int = 0) -> np
                             threads):
         raise ValueError("oracle gemm: bad arguments")
     return y
+
+
+def silu_f64(g: float) -> float:
+    """silu(g) = g / (1 + e^-g) in double."""
+    return _load().wqo_silu_f64(float(g))
+
+
+def swiglu_bf16(y: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns [M][N/2] of silu(y[:, 2j]) * y[:, 2j + 1], one rounding."""
+    y = np.ascontiguousarray(y, dtype=np.float64)
+    M, N = y.shape
+    out = np.empty((M, N // 2), dtype=np.uint16)
+    rc = _load().wqo_swiglu_bf16(_ptr(y), M, N, _ptr(out))
+    if rc:
+        raise ValueError("swiglu_bf16: N must be even")
+    return out
 
 
 def max_threads(threads: int = 0) -> int:

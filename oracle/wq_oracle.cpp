@@ -36,6 +36,14 @@
 //     - scales are bf16 [N][K/G], zero points uint8 [N][K/G], both row-major;
 //     - X is bf16 [M][K] row-major, Y is [M][N] row-major.
 //
+// Fused gate/up activation (wqo_silu_f64, wqo_swiglu_bf16): the pages run
+// Qwen-family models (OpenJet news page, title: Qwen3.8-27B) and fuse a
+// layer's gate and up projections into one weight stream, but never write the
+// activation.  Reading: the gated SiLU unit of those models,
+// out[m][j] = silu(gate) * up with silu(g) = g / (1 + e^-g), the gate and up
+// rows of feature j interleaved as rows 2j and 2j + 1 of the fused
+// projection, rounded once to bf16 (the next projection's X is bf16).
+//
 // Precision: q - z is an integer of magnitude < 2^8 and s is a bf16 (8
 // significant bits), so W is exact in double; X is bf16, so each product is
 // exact and only the K-term sum rounds (in double, k ascending).
@@ -144,6 +152,21 @@ uint16_t wqo_bf16_rne(double v) {
     uint32_t u;
     std::memcpy(&u, &f, sizeof u);
     return static_cast<uint16_t>(u >> 16);  // low 16 bits are zero
+}
+
+// SiLU, written from its definition: g * sigmoid(g) = g / (1 + e^-g).
+double wqo_silu_f64(double g) { return g / (1.0 + std::exp(-g)); }
+
+// out[m][j] = bf16(silu(y[m][2j]) * y[m][2j + 1]) for y [M][N] in double
+// (N even), one rounding of the double product.  Domain of wqo_bf16_rne:
+// products that are 0 or in the normal bf16 range.
+int wqo_swiglu_bf16(const double* y, int M, int N, uint16_t* out) {
+    if (M < 0 || N < 0 || N % 2 != 0) return 1;
+    const long nf = N / 2;
+    for (long m = 0; m < M; ++m)
+        for (long j = 0; j < nf; ++j)
+            out[m * nf + j] = wqo_bf16_rne(wqo_silu_f64(y[m * N + 2 * j]) * y[m * N + 2 * j + 1]);
+    return 0;
 }
 
 // bf16(W) with a single rounding of the exact product.

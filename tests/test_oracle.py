@@ -275,3 +275,39 @@ def test_step_floor_matches_printed_figure(golden_dir):
     t_ms = oracle.step_floor_seconds(float(inp[0]), float(inp[1])) * 1e3
     assert abs(t_ms - float(out[0])) <= float(out[1])
     assert abs(t_ms - 17.842) < 1e-3
+
+
+# ------------------------------------------------------------ fused SwiGLU
+def test_swiglu_golden_values(golden_dir):
+    rows = _read_golden(os.path.join(golden_dir, "swiglu_bf16.txt"))
+    assert len(rows) >= 6
+    for (inp, out, _why) in rows:
+        g, u = float(inp[0]), float(inp[1])
+        y = np.array([[g, u]], dtype=np.float64)
+        assert int(oracle.swiglu_bf16(y)[0, 0]) == int(out[0], 16), (inp, hex(int(oracle.swiglu_bf16(y)[0, 0])))
+
+
+def test_silu_closed_forms():
+    # silu(x) - silu(-x) = x (sigmoid(x) + sigmoid(-x) = 1); silu(0) = 0;
+    # silu(x) -> x and silu(-x) -> -x e^-x as x grows
+    for x in (0.25, 1.0, 3.5, 7.0, 12.0):
+        assert abs((oracle.silu_f64(x) - oracle.silu_f64(-x)) - x) <= 4e-16 * x
+    assert oracle.silu_f64(0.0) == 0.0
+    assert oracle.silu_f64(40.0) == 40.0
+    assert abs(oracle.silu_f64(-40.0) / (-40.0 * np.exp(-40.0)) - 1.0) < 1e-15
+    # sigmoid(x) = silu(x) / x is the logistic function: 1/2 at 0+, e/(1+e) at 1
+    assert abs(oracle.silu_f64(1.0) - np.e / (1.0 + np.e)) < 1e-16
+
+
+def test_swiglu_layout_pairs_rows_and_rejects_odd_widths():
+    # column 2j is the gate and 2j + 1 the up value of feature j; swapping them
+    # changes the result, and an odd width is refused
+    y = np.array([[2.0, 1.0, 1.0, 2.0], [-3.0, 0.25, 0.0, 9.0]])
+    out = oracle.swiglu_bf16(y)
+    assert out.shape == (2, 2)
+    assert out[0, 0] == oracle.bf16_rne(oracle.silu_f64(2.0) * 1.0)
+    assert out[0, 1] == oracle.bf16_rne(oracle.silu_f64(1.0) * 2.0)
+    assert out[0, 0] != out[0, 1]
+    assert out[1, 1] == 0  # silu(0) * 9 = 0
+    with pytest.raises(ValueError):
+        oracle.swiglu_bf16(np.zeros((1, 3)))
