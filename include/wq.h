@@ -127,6 +127,28 @@ wq_status_t wq_gemm(const uint16_t* x, const uint32_t* wq, const uint16_t* scale
                     const uint8_t* zeros, float* y, int M, int N, int K, int group, int bits,
                     void* workspace, size_t workspace_bytes, void* stream);
 
+/* Epilogues: what a projection writes from its fp32 sums acc[M][N]. */
+#define WQ_EPI_NONE 0   /* y: fp32 [M][N] = acc */
+#define WQ_EPI_SWIGLU 1 /* y: bf16 [M][N/2], y[m][j] = bf16(silu(acc[m][2j]) * acc[m][2j+1]) */
+
+/*
+ * wq_gemm_swiglu — the fused gate/up projection of a gated MLP with its
+ * activation applied in the epilogue: y[m][j] = RNE_bf16(silu(g) * u) with
+ * g = acc[m][2j], u = acc[m][2j+1], silu(g) = g / (1 + e^-g) in fp32, acc the
+ * wq_gemm sums.  The pages fuse gate and up into one weight stream (OpenJet
+ * news page, "并行解码的原理": one pass over every weight per step) for
+ * Qwen-family models without naming the activation; SwiGLU is the reading.
+ * Layout: N even; weight rows (and their scale and zero-point rows) are
+ * interleaved at load time, row 2j = gate row of feature j, row 2j + 1 = up
+ * row; y is bf16 [M][N/2] row-major (the down projection's X), 2-byte
+ * aligned.  Everything else (x, wq, scales, zeros, workspace, errors) as
+ * wq_gemm; the fp32 sums are those of wq_gemm bit for bit, so y equals the
+ * activation applied to wq_gemm's output up to the last bit of expf.
+ */
+wq_status_t wq_gemm_swiglu(const uint16_t* x, const uint32_t* wq, const uint16_t* scales,
+                           const uint8_t* zeros, uint16_t* y, int M, int N, int K, int group,
+                           int bits, void* workspace, size_t workspace_bytes, void* stream);
+
 /*
  * wq_gemm_noalloc — wq_gemm without any device allocation.  The paper has no
  * counterpart: this entry point exists for callers that cannot call cudaMalloc,
@@ -172,7 +194,7 @@ typedef struct wq_proj_desc {
     const uint32_t* wq;      /* [N][W] */
     const uint16_t* scales;  /* [N][K/G] bf16 */
     const uint8_t* zeros;    /* [N][K/G] */
-    float* y;                /* [M][N] fp32 */
+    void* y;                 /* fp32 [M][N]; bf16 [M][N/2] with WQ_EPI_SWIGLU */
     int M, N, K, group, bits;
     /* Fused mode only: x is produced by projections 0..after of the same
      * call (through whatever the caller computes in between), so it is read
@@ -180,6 +202,9 @@ typedef struct wq_proj_desc {
      * starts.  Must be smaller than the projection's own index.  Ignored in
      * sequential mode, where stream order already serialises everything. */
     int after;
+    /* WQ_EPI_NONE: y is fp32 [M][N]; WQ_EPI_SWIGLU: y is bf16 [M][N/2] as in
+     * wq_gemm_swiglu (N even, gate/up rows interleaved). */
+    int epilogue;
 } wq_proj_desc_t;
 
 /* Step modes.

@@ -34,7 +34,7 @@ def test_every_declared_symbol_is_exported(wq):
 
 
 def test_abi_version_and_words(wq):
-    assert wq.abi_version() == 101
+    assert wq.abi_version() == 102
     assert wq.wq_packed_words_per_row(17408, 3) == 1744
     assert wq.wq_packed_words_per_row(5120, 4) == 640
     assert wq.wq_packed_words_per_row(17408, 2) == 1088

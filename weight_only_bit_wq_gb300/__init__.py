@@ -24,12 +24,14 @@ WQ_OK, WQ_ERR_INVALID_ARG, WQ_ERR_UNSUPPORTED, WQ_ERR_CUDA, WQ_ERR_TIMEOUT = ran
 
 EXPORTED = ("wq_abi_version", "wq_status_string", "wq_last_cuda_error", "wq_packed_words_per_row",
             "wq_pack", "wq_unpack", "wq_dequant", "wq_workspace_bytes", "wq_workspace_init",
-            "wq_gemm", "wq_check_workspace", "wq_step_workspace_bytes", "wq_step_run",
+            "wq_gemm", "wq_gemm_swiglu", "wq_check_workspace", "wq_step_workspace_bytes", "wq_step_run",
             "wq_step_run_ex", "wq_step_graph_create", "wq_step_graph_create_ex",
             "wq_step_graph_launch", "wq_step_graph_destroy")
 
 # Step modes (include/wq.h).
 WQ_STEP_FUSED = 1
+# Projection epilogues (include/wq.h).
+WQ_EPI_NONE, WQ_EPI_SWIGLU = 0, 1
 
 
 class WQError(RuntimeError):
@@ -46,7 +48,7 @@ class ProjDesc(ctypes.Structure):
     _fields_ = [("x", ctypes.c_void_p), ("wq", ctypes.c_void_p), ("scales", ctypes.c_void_p),
                 ("zeros", ctypes.c_void_p), ("y", ctypes.c_void_p), ("M", ctypes.c_int),
                 ("N", ctypes.c_int), ("K", ctypes.c_int), ("group", ctypes.c_int),
-                ("bits", ctypes.c_int), ("after", ctypes.c_int)]
+                ("bits", ctypes.c_int), ("after", ctypes.c_int), ("epilogue", ctypes.c_int)]
 
 
 _LIB: Optional[ctypes.CDLL] = None
@@ -70,6 +72,7 @@ def _lib() -> ctypes.CDLL:
             "wq_workspace_bytes": ([I, I, I, I, I], S),
             "wq_workspace_init": ([P, S, P], I),
             "wq_gemm": ([P, P, P, P, P, I, I, I, I, I, P, S, P], I),
+            "wq_gemm_swiglu": ([P, P, P, P, P, I, I, I, I, I, P, S, P], I),
             "wq_check_workspace": ([P, P], I),
             "wq_step_workspace_bytes": ([P, I, ctypes.c_uint], S),
             "wq_step_run": ([P, I, P, S, P], I),
@@ -174,6 +177,20 @@ def wq_gemm(x, wq, scales, zeros, N: int, group: int, bits: int, out=None, works
     return out
 
 
+def wq_gemm_swiglu(x, wq, scales, zeros, N: int, group: int, bits: int, out=None, workspace=None,
+                   stream=None) -> torch.Tensor:
+    """bf16 [M][N/2] = silu(gate) * up of the fused gate/up projection (rows 2j, 2j + 1 of the
+    weights are the gate and up rows of feature j)."""
+    M, K = x.shape
+    if out is None:
+        out = torch.empty((M, N // 2), dtype=torch.bfloat16, device=x.device)
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(_lib().wq_gemm_swiglu(_ptr(x), _ptr(wq), _ptr(scales), _ptr(zeros), _ptr(out), M, N, K,
+                                 group, bits, _ptr(workspace), nbytes, _stream(stream)),
+           "wq_gemm_swiglu")
+    return out
+
+
 def wq_check_workspace(workspace=None, stream=None) -> None:
     _check(_lib().wq_check_workspace(_ptr(workspace), _stream(stream)), "wq_check_workspace")
 
@@ -185,7 +202,7 @@ def make_descs(projs: Sequence[dict]) -> ctypes.Array:
     for i, p in enumerate(projs):
         arr[i] = ProjDesc(p["x"].data_ptr(), p["wq"].data_ptr(), p["scales"].data_ptr(),
                           p["zeros"].data_ptr(), p["y"].data_ptr(), p["M"], p["N"], p["K"],
-                          p["group"], p["bits"], p.get("after", -1))
+                          p["group"], p["bits"], p.get("after", -1), p.get("epilogue", WQ_EPI_NONE))
     return arr
 
 

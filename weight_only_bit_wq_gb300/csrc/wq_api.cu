@@ -103,7 +103,7 @@ int choose_grid(int T, int I, int sm_count) {
 
 extern "C" {
 
-int wq_abi_version(void) { return 101; }
+int wq_abi_version(void) { return 102; }
 
 const char* wq_status_string(wq_status_t s) {
     switch (s) {
@@ -266,13 +266,15 @@ wq_status_t host_sm_count(int* sms) {
 }
 
 wq_status_t host_check_gemm(const uint16_t* x, const uint32_t* wq, const uint16_t* scales,
-                            const uint8_t* zeros, const float* y, int M, int N, int K, int group,
-                            int bits) {
+                            const uint8_t* zeros, const void* y, int M, int N, int K, int group,
+                            int bits, int epi) {
     if (!valid_bits(bits) || !valid_group(group) || M < 0 || M > kMaxCols || N < 0 || K < 0 ||
         K % group != 0)
         return WQ_ERR_INVALID_ARG;
+    if (epi != WQ_EPI_NONE && epi != WQ_EPI_SWIGLU) return WQ_ERR_INVALID_ARG;
+    if (epi == WQ_EPI_SWIGLU && N % 2 != 0) return WQ_ERR_INVALID_ARG;
     if (M == 0 || N == 0) return WQ_OK;
-    if (!y || !aligned(y, 4)) return WQ_ERR_INVALID_ARG;
+    if (!y || !aligned(y, epi == WQ_EPI_SWIGLU ? 2 : 4)) return WQ_ERR_INVALID_ARG;
     if (K == 0) return WQ_OK;
     if (!x || !wq || !scales || !zeros || !aligned(x, 16) || !aligned(wq, 16) || !aligned(scales, 2))
         return WQ_ERR_INVALID_ARG;
@@ -300,14 +302,17 @@ wq_status_t host_encode_proj(const uint16_t* x, const uint32_t* wq, const uint16
 namespace wq {
 
 wq_status_t gemm_run(const uint16_t* x, const uint32_t* wq, const uint16_t* scales,
-                     const uint8_t* zeros, float* y, int M, int N, int K, int group, int bits,
-                     void* workspace, size_t workspace_bytes, cudaStream_t s, bool pdl) {
-    if (wq_status_t st = host_check_gemm(x, wq, scales, zeros, y, M, N, K, group, bits))
+                     const uint8_t* zeros, void* y, int M, int N, int K, int group, int bits,
+                     void* workspace, size_t workspace_bytes, cudaStream_t s, bool pdl,
+                     int epi) {
+    if (wq_status_t st = host_check_gemm(x, wq, scales, zeros, y, M, N, K, group, bits, epi))
         return st;
     if (M == 0 || N == 0) return WQ_OK;
 
-    if (K == 0) {  // empty sum
-        cudaError_t e = cudaMemsetAsync(y, 0, static_cast<size_t>(M) * N * sizeof(float), s);
+    if (K == 0) {  // empty sum: fp32 zeros, or silu(0) * 0 = +0 in bf16
+        const size_t bytes = epi == WQ_EPI_SWIGLU ? static_cast<size_t>(M) * (N / 2) * 2
+                                                  : static_cast<size_t>(M) * N * sizeof(float);
+        cudaError_t e = cudaMemsetAsync(y, 0, bytes, s);
         return e == cudaSuccess ? WQ_OK : cuda_fail(e);
     }
     DeviceInfo* d;
@@ -331,7 +336,8 @@ wq_status_t gemm_run(const uint16_t* x, const uint32_t* wq, const uint16_t* scal
         return st;
     a.scales = scales;
     a.zeros = zeros;
-    a.y = y;
+    a.y = static_cast<float*>(y);
+    a.epi = epi;
     uint8_t* wsb = static_cast<uint8_t*>(ws);
     a.err = reinterpret_cast<int*>(wsb);
     a.partials = reinterpret_cast<float*>(wsb + lay.partial_off);
@@ -365,7 +371,14 @@ wq_status_t wq_gemm(const uint16_t* x, const uint32_t* wq, const uint16_t* scale
                     const uint8_t* zeros, float* y, int M, int N, int K, int group, int bits,
                     void* workspace, size_t workspace_bytes, void* stream) {
     return wq::gemm_run(x, wq, scales, zeros, y, M, N, K, group, bits, workspace, workspace_bytes,
-                        as_stream(stream), false);
+                        as_stream(stream), false, WQ_EPI_NONE);
+}
+
+wq_status_t wq_gemm_swiglu(const uint16_t* x, const uint32_t* wq, const uint16_t* scales,
+                           const uint8_t* zeros, uint16_t* y, int M, int N, int K, int group,
+                           int bits, void* workspace, size_t workspace_bytes, void* stream) {
+    return wq::gemm_run(x, wq, scales, zeros, y, M, N, K, group, bits, workspace, workspace_bytes,
+                        as_stream(stream), false, WQ_EPI_SWIGLU);
 }
 wq_status_t wq_check_workspace(void* workspace, void* stream) {
     void* ws = workspace;

@@ -36,6 +36,7 @@
 // so a row of X gives bit-identical results alone or stacked.  A tile split
 // across CTAs is summed by the last CTA to finish it, in k order.
 #pragma once
+#include <cuda_bf16.h>
 #include <type_traits>
 
 #include "wq_internal.h"
@@ -436,7 +437,7 @@ struct ProjView {
     const uint8_t* zeros;
     float* y;
     long long uoff;  // first global unit
-    int M, N, ng, T, I, toff, after, phase;
+    int M, N, ng, T, I, toff, after, phase, epi;
     bool meta_vec, x3d;
 };
 
@@ -472,6 +473,7 @@ struct Ctx {
         v.toff = d.toff;
         v.after = d.after;
         v.phase = d.phase;
+        v.epi = d.epi;
         v.meta_vec = d.meta_vec != 0;
         v.x3d = d.x3d != 0;
         return v;
@@ -563,6 +565,38 @@ struct Cursor {
     }
 };
 
+// Epilogue kinds a kernel is built for: fp32 Y only, the fused gate/up
+// activation only, or either (chosen per projection at run time).
+constexpr int kEpiY = 0, kEpiAct = 1, kEpiAny = 2;
+
+// Final values of tile row n (this lane) for all rows of X: fp32 Y, or, for
+// the fused gate/up projection, the activation: rows 2j and 2j + 1 (gate and
+// up of feature j) are neighbouring lanes, and the even lane stores
+// bf16(silu(gate) * up) at column j of the bf16 [M][N/2] output.
+template <int EPI>
+__device__ __forceinline__ void store_final(const ProjView& v, int n, const float (&val)[kN],
+                                            int lane) {
+    if (EPI == kEpiY || (EPI == kEpiAny && v.epi == WQ_EPI_NONE)) {
+        if (n < v.N)
+#pragma unroll
+            for (int j = 0; j < kN; ++j)
+                if (j < v.M) v.y[static_cast<size_t>(j) * v.N + n] = val[j];
+        return;
+    }
+    if constexpr (EPI != kEpiY) {
+        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(v.y);
+        const int nf = v.N >> 1, f = n >> 1;
+        const bool even = (lane & 1) == 0 && n < v.N;
+#pragma unroll
+        for (int j = 0; j < kN; ++j) {
+            const float g = val[j];
+            const float u = __shfl_xor_sync(kFull, g, 1);
+            if (even && j < v.M)
+                out[static_cast<size_t>(j) * nf + f] = __float2bfloat16_rn(g / (1.0f + expf(-g)) * u);
+        }
+    }
+}
+
 // End of a tile segment for one epilogue warp (rows 32 q + lane, all
 // accumulator columns): store Y, or publish the partial sums and let the
 // warp of the last CTA to finish the tile add all partials in k order.  Each
@@ -574,6 +608,7 @@ struct Cursor {
 //   of their shares, so they have usually all arrived already.  Then the
 //   warp checks the counter first and, if they have, sums at once without
 //   publishing its own partial (two round trips fewer at the end of a share).
+template <int EPI>
 __device__ __forceinline__ void finish_rows(const Ctx& c, const ProjView& v,
                                             const float (&acc)[kN], int t, bool whole,
                                             bool likely_last, int r, int q, int lane) {
@@ -586,10 +621,7 @@ __device__ __forceinline__ void finish_rows(const Ctx& c, const ProjView& v,
         }
     };
     if (whole) {
-        if (n < v.N)
-#pragma unroll
-            for (int j = 0; j < kN; ++j)
-                if (j < v.M) v.y[static_cast<size_t>(j) * v.N + n] = acc[j];
+        store_final<EPI>(v, n, acc, lane);
         count_done();
         return;
     }
@@ -643,10 +675,7 @@ __device__ __forceinline__ void finish_rows(const Ctx& c, const ProjView& v,
             for (int j = 0; j < kN; ++j) tot[j] += part[j];
         }
     }
-    if (n < v.N)
-#pragma unroll
-        for (int j = 0; j < kN; ++j)
-            if (j < v.M) v.y[static_cast<size_t>(j) * v.N + n] = tot[j];
+    store_final<EPI>(v, n, tot, lane);
     if (lane == 0) *ctr = 0;
     count_done();
 }
@@ -764,7 +793,7 @@ __device__ __forceinline__ void unpack_warp(const Ctx& c, uint32_t smem_u32, B& 
 // Epilogue warp (lane quarter q).  Per unit it reads the unit's two batches
 // of accumulators back (adding scale * D to the row's 16 fp32 sums) and ends
 // tile segments.
-template <int BITS, int G, class B>
+template <int BITS, int G, int EPI, class B>
 __device__ __forceinline__ void epilogue_warp(const Ctx& c, B& bars, uint32_t tmem,
                                               volatile int* abort_flag, int q, int lane,
                                               int n_units) {
@@ -835,7 +864,7 @@ __device__ __forceinline__ void epilogue_warp(const Ctx& c, B& bars, uint32_t tm
         const bool end = tile_end || cc.last_of_share();
         if (end) {
             if (!dead)
-                finish_rows(c, cc.v, acc, cc.t, seg_from_start && tile_end,
+                finish_rows<EPI>(c, cc.v, acc, cc.t, seg_from_start && tile_end,
                             seg_from_start && !tile_end, r, q, lane);
 #pragma unroll
             for (int j = 0; j < kN; ++j) acc[j] = 0.f;
@@ -873,7 +902,7 @@ __device__ __forceinline__ bool wait_deps(const Ctx& c, int upto, int& verified,
     }
 }
 
-template <int BITS, int G, bool MULTI>
+template <int BITS, int G, bool MULTI, int EPI>
 __global__ void __launch_bounds__(Lay<BITS, G>::kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                    const GemmArgs a, const StepArgs sa) {
@@ -918,6 +947,7 @@ __global__ void __launch_bounds__(Lay<BITS, G>::kThreads, 1)
         c.one.toff = 0;
         c.one.after = -1;
         c.one.phase = 0;
+        c.one.epi = a.epi;
         c.one.meta_vec = a.meta_vec != 0;
         c.one.x3d = a.x3d != 0;
         c.partials = a.partials;
@@ -1216,7 +1246,7 @@ __global__ void __launch_bounds__(Lay<BITS, G>::kThreads, 1)
 
     if (warp >= L::kUW) {
         // ------------------------------------------------------------ epilogue
-        epilogue_warp<BITS, G>(c, bars, tmem, abort_flag, warp & 3, lane, n_units);
+        epilogue_warp<BITS, G, EPI>(c, bars, tmem, abort_flag, warp & 3, lane, n_units);
     } else if constexpr (BITS == 3) {
         // ------------------------------------------------------------ unpack
         static_for<0, L::kSplit>([&](auto hc) {
@@ -1234,7 +1264,8 @@ template <int BITS, int G>
 cudaError_t launch_tc(const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmArgs& a,
                       cudaStream_t s) {
     using L = Lay<BITS, G>;
-    auto kern = gemm_tc_kernel<BITS, G, false>;
+    auto kern = a.epi == WQ_EPI_SWIGLU ? gemm_tc_kernel<BITS, G, false, kEpiAct>
+                                       : gemm_tc_kernel<BITS, G, false, kEpiY>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
     if (e != cudaSuccess) return e;
@@ -1258,9 +1289,9 @@ cudaError_t launch_tc(const CUtensorMap& tmW, const CUtensorMap& tmX, const Gemm
 // Fused step launch; cooperative (all CTAs resident at once) when projections
 // wait for one another.
 template <int BITS, int G>
-cudaError_t launch_step(const StepArgs& sa, bool cooperative, cudaStream_t s) {
+cudaError_t launch_step(const StepArgs& sa, bool cooperative, bool any_act, cudaStream_t s) {
     using L = Lay<BITS, G>;
-    auto kern = gemm_tc_kernel<BITS, G, true>;
+    auto kern = any_act ? gemm_tc_kernel<BITS, G, true, kEpiAny> : gemm_tc_kernel<BITS, G, true, kEpiY>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
     if (e != cudaSuccess) return e;

@@ -42,6 +42,7 @@ struct GemmArgs {
     int x3d;          // X map is 3-D [K/64][M][64]: one TMA box per stage (K % 64 == 0)
     int pdl;          // launched as a programmatic dependent of the previous kernel on the
                       // stream: X is read, and anything written, once that kernel completed
+    int epi;          // WQ_EPI_NONE or WQ_EPI_SWIGLU (y is then bf16 [M][N/2])
 };
 
 // One projection of a fused step, as the step kernel reads it from device
@@ -59,7 +60,8 @@ struct ProjDev {  // aligned like its tensor maps
     int meta_vec, x3d;
     int after;               // X is read once phase `after` of this launch is complete (-1: at once)
     int phase;               // phase of the launch this projection belongs to
-    int pad[4];
+    int epi;                 // WQ_EPI_NONE or WQ_EPI_SWIGLU (y is then bf16 [M][N/2])
+    int pad[3];
 };
 
 // A phase of a fused step: consecutive projections none of which waits for
@@ -100,24 +102,29 @@ cudaError_t launch_gemm_tc_b3(int group, const CUtensorMap& tmW, const CUtensorM
 cudaError_t launch_gemm_tc_b2(int group, const CUtensorMap& tmW, const CUtensorMap& tmX,
                               const GemmArgs& a, cudaStream_t s);
 // Fused step: all projections of `sa` (one bit width and group size) in one
-// persistent launch; cooperative when any projection waits for another.
-cudaError_t launch_step_b4(int group, const StepArgs& sa, bool cooperative, cudaStream_t s);
-cudaError_t launch_step_b3(int group, const StepArgs& sa, bool cooperative, cudaStream_t s);
-cudaError_t launch_step_b2(int group, const StepArgs& sa, bool cooperative, cudaStream_t s);
+// persistent launch; cooperative when any projection waits for another;
+// any_act: some projection has the fused gate/up activation epilogue.
+cudaError_t launch_step_b4(int group, const StepArgs& sa, bool cooperative, bool any_act,
+                           cudaStream_t s);
+cudaError_t launch_step_b3(int group, const StepArgs& sa, bool cooperative, bool any_act,
+                           cudaStream_t s);
+cudaError_t launch_step_b2(int group, const StepArgs& sa, bool cooperative, bool any_act,
+                           cudaStream_t s);
 
 // wq_gemm with the launch mode chosen by the caller: pdl = launch as a
 // programmatic dependent of the previous kernel on the stream (only where
 // that kernel writes none of wq, scales and zeros).
 wq_status_t gemm_run(const uint16_t* x, const uint32_t* wq, const uint16_t* scales,
-                     const uint8_t* zeros, float* y, int M, int N, int K, int group, int bits,
-                     void* workspace, size_t workspace_bytes, cudaStream_t s, bool pdl);
+                     const uint8_t* zeros, void* y, int M, int N, int K, int group, int bits,
+                     void* workspace, size_t workspace_bytes, cudaStream_t s, bool pdl,
+                     int epi);
 
 // Host helpers shared by the entry points (wq_api.cu).
 wq_status_t host_cuda_fail(cudaError_t e);
 wq_status_t host_sm_count(int* sms);
 wq_status_t host_check_gemm(const uint16_t* x, const uint32_t* wq, const uint16_t* scales,
-                            const uint8_t* zeros, const float* y, int M, int N, int K, int group,
-                            int bits);
+                            const uint8_t* zeros, const void* y, int M, int N, int K, int group,
+                            int bits, int epi);
 wq_status_t host_encode_proj(const uint16_t* x, const uint32_t* wq, const uint16_t* scales,
                              const uint8_t* zeros, int M, int N, int K, int group, int bits,
                              CUtensorMap* tmW, CUtensorMap* tmX, int* x3d, int* meta_vec);

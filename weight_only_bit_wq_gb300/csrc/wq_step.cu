@@ -94,7 +94,7 @@ wq_status_t check_all(const wq_proj_desc_t* projs, int count) {
     for (int i = 0; i < count; ++i) {
         const wq_proj_desc_t& p = projs[i];
         if (wq_status_t st = wq::host_check_gemm(p.x, p.wq, p.scales, p.zeros, p.y, p.M, p.N, p.K,
-                                                 p.group, p.bits))
+                                                 p.group, p.bits, p.epilogue))
             return st;
         if (p.after >= i || p.after < -1) return WQ_ERR_INVALID_ARG;
     }
@@ -132,7 +132,8 @@ wq_status_t build_table(const wq_proj_desc_t* projs, const Run& r, std::vector<w
         }
         d.scales = p.scales;
         d.zeros = p.zeros;
-        d.y = p.y;
+        d.y = static_cast<float*>(p.y);
+        d.epi = p.epilogue;
         d.M = p.M;
         d.N = p.N;
         d.ng = p.K / p.group;
@@ -156,7 +157,8 @@ wq_status_t build_table(const wq_proj_desc_t* projs, const Run& r, std::vector<w
 
 // Reset the run's completion counters and launch its persistent kernel.
 wq_status_t launch_run(const Run& r, Tables tab, int nphase, long long units, bool waits,
-                       uint8_t* ws, const FusedLayout& lay, int sms, cudaStream_t s) {
+                       bool any_act, uint8_t* ws, const FusedLayout& lay, int sms,
+                       cudaStream_t s) {
     const int n = r.end - r.begin;
     int* done = reinterpret_cast<int*>(ws + lay.done_off);
     cudaError_t e = cudaMemsetAsync(done, 0, static_cast<size_t>(n) * sizeof(int), s);
@@ -173,18 +175,18 @@ wq_status_t launch_run(const Run& r, Tables tab, int nphase, long long units, bo
     sa.U = units;
     sa.P = static_cast<int>(std::min<long long>(sms, units));
     if (r.bits == 4)
-        e = wq::launch_step_b4(r.group, sa, waits, s);
+        e = wq::launch_step_b4(r.group, sa, waits, any_act, s);
     else if (r.bits == 3)
-        e = wq::launch_step_b3(r.group, sa, waits, s);
+        e = wq::launch_step_b3(r.group, sa, waits, any_act, s);
     else
-        e = wq::launch_step_b2(r.group, sa, waits, s);
+        e = wq::launch_step_b2(r.group, sa, waits, any_act, s);
     return e == cudaSuccess ? WQ_OK : wq::host_cuda_fail(e);
 }
 
 wq_status_t run_single(const wq_proj_desc_t& p, void* workspace, size_t workspace_bytes,
                        cudaStream_t s, bool pdl = false) {
     return wq::gemm_run(p.x, p.wq, p.scales, p.zeros, p.y, p.M, p.N, p.K, p.group, p.bits,
-                        workspace, workspace_bytes, s, pdl);
+                        workspace, workspace_bytes, s, pdl, p.epilogue);
 }
 
 bool launches_kernel(const wq_proj_desc_t& p) { return p.M > 0 && p.N > 0 && p.K > 0; }
@@ -259,8 +261,10 @@ wq_status_t run_fused(const wq_proj_desc_t* projs, int count, void* workspace,
                                     phases.size() * sizeof(wq::PhaseDev), cudaMemcpyHostToDevice, s);
             if (e != cudaSuccess) return wq::host_cuda_fail(e);
         }
-        if (wq_status_t st = launch_run(r, tab, static_cast<int>(phases.size()), units, waits, ws,
-                                        lay, sms, s))
+        bool any_act = false;
+        for (int i = r.begin; i < r.end; ++i) any_act = any_act || projs[i].epilogue != WQ_EPI_NONE;
+        if (wq_status_t st = launch_run(r, tab, static_cast<int>(phases.size()), units, waits,
+                                        any_act, ws, lay, sms, s))
             return st;
     }
     return WQ_OK;
