@@ -3,14 +3,17 @@
 
 One "step" is one decode step of a 64-layer projection stack (q, k, v, o,
 fused gate/up and down of a 5120-hidden / 17408-FFN decoder, 4-bit codes,
-group 128): 384 wq_gemm launches replayed as one CUDA graph, every packed
-weight streamed from HBM once (11.08 GB of weights, scales and zero points,
-far larger than the 129 MB L2, so no flush is needed between steps).
+group 128): one fused persistent launch (WQ_STEP_FUSED) honouring the layer
+dependency chain, replayed as a CUDA graph, every packed weight streamed from
+HBM once (11.08 GB of weights, scales and zero points, far larger than the
+129 MB L2, so no flush is needed between steps).
 
 The JSON line reports the effective weight-stream bandwidth (packed weight
-bytes / step time) at the headline row count, the M sweep, per-config
-single-call figures, the dominant kernel's roofline, an end-to-end figure
-through the C ABI with host buffers, and the CPU oracle baseline.
+bytes / step time) at the headline row count, the M sweep, the same step in
+other modes (with the gate/up activation feeding down, without dependencies,
+one launch per projection), per-config single-call figures, the dominant
+kernel's roofline, an end-to-end figure through the C ABI with host buffers,
+and the CPU oracle baseline.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -317,8 +320,9 @@ def count_runs(descs):
 
 def run_sweep_point(stack, M, stream, steps, warmup, dist, clocks=None, e2e=False, mode="fused"):
     """ms per step of the whole stack, as one CUDA graph: fused (one persistent launch per
-    step, honouring the layer dependency chain), fused-independent (no dependencies) or
-    sequential (one launch per projection)."""
+    step, honouring the layer dependency chain), fused-swiglu (the same, with each gate/up
+    projection's epilogue writing silu(gate) * up as the down projection's bf16 X),
+    fused-independent (no dependencies) or sequential (one launch per projection)."""
     import torch
 
     wq = stack.wq
@@ -326,6 +330,14 @@ def run_sweep_point(stack, M, stream, steps, warmup, dist, clocks=None, e2e=Fals
     if mode == "fused-independent":
         for d in descs:
             d["after"] = -1
+    if mode == "fused-swiglu":
+        for i, p in enumerate(stack.projs):
+            if p.name.endswith("gate_up"):
+                act = torch.empty((M, p.N // 2), dtype=torch.bfloat16, device=stack.device)
+                descs[i]["y"] = act
+                descs[i]["epilogue"] = wq.WQ_EPI_SWIGLU
+                assert stack.projs[i + 1].name.endswith("down") and descs[i + 1]["K"] == p.N // 2
+                descs[i + 1]["x"] = act
     cd = wq.make_descs(descs)
     stream.wait_stream(torch.cuda.current_stream())
     if mode == "sequential":
@@ -531,7 +543,7 @@ def main_ours(args):
                           "roofline_frac": round(b["total"] / (ms * 1e-3) / 1e9 / peak, 4)})
     # the same step without dependencies, and as one launch per projection
     modes = {}
-    for mode in ("fused-independent", "sequential"):
+    for mode in ("fused-swiglu", "fused-independent", "sequential"):
         r = run_sweep_point(stack, args.m, stream, max(3, args.steps // 4), 2, dist, mode=mode)
         ms = reduce_max(dist, r["ms_per_step"], device)
         modes[mode] = {"ms_per_step": round(ms, 4), "launches_per_step": r["launches_per_step"],

@@ -83,6 +83,39 @@ def test_swiglu_rows_are_batch_invariant():
         assert (alone[0] == full[m]).all(), m
 
 
+def test_swiglu_saturating_gates():
+    # Gate values from far below the fp32 exponential's range to well above
+    # it.  Down to about -87 the result matches the oracle to one bf16 step;
+    # below, the device's 1 + exp(-g) passes 2^126 and its quotient is zero,
+    # where the exact value is under 1e-36 times |up| in magnitude.
+    import weight_only_bit_wq_gb300 as wq
+    targets = [-150.0, -100.0, -88.0, -87.5, -80.0, -10.0, 0.25, 60.0]
+    F, K, G, M = len(targets), 256, 128, 2
+    N = 2 * F
+    q = np.full((N, K), 15, dtype=np.uint8)
+    z = np.zeros((N, K // G), dtype=np.uint8)
+    s32 = np.empty((N, K // G), dtype=np.float32)
+    s32[0::2] = (np.array(targets, dtype=np.float32) / (15 * K))[:, None]
+    s32[1::2] = np.float32(2.0 / (15 * K))
+    s = synth.f32_to_bf16_bits(s32)
+    x = synth.f32_to_bf16_bits(np.array([[1.0] * K, [0.5] * K], dtype=np.float32))
+    d = dev()
+    out = wq.wq_gemm_swiglu(torch.from_numpy(x.view(np.int16)).to(d),
+                            wq.wq_pack(torch.from_numpy(q).to(d), 4),
+                            torch.from_numpy(s.view(np.int16)).to(d), torch.from_numpy(z).to(d),
+                            N, G, 4)
+    got = _bits(out)
+    y64 = oracle.gemm_f64(x, oracle.pack(q, 4), s, z, K, G, 4)
+    ref = oracle.swiglu_bf16(y64)
+    g = y64[:, 0::2]
+    normal = g > -87.0
+    assert normal.sum() >= 10 and (~normal).sum() >= 3
+    assert _ulps(got[normal], ref[normal]) <= 1
+    assert ((got[~normal] & 0x7FFF) == 0).all()
+    ref_f = synth.bf16_bits_to_f32(ref[~normal])
+    assert (np.abs(ref_f) < 1e-35).all()
+
+
 def test_swiglu_rejects_odd_width_and_handles_empty_k():
     import weight_only_bit_wq_gb300 as wq
     p = synth.Projection("gu4", 2, 256, 256, 4, 128, 604)

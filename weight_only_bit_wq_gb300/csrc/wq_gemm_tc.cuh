@@ -566,13 +566,15 @@ struct Cursor {
 };
 
 // Epilogue kinds a kernel is built for: fp32 Y only, the fused gate/up
-// activation only, or either (chosen per projection at run time).
+// activation only, or either (chosen per projection at run time).  Single
+// GEMMs take the first two; a fused step always takes the third, which
+// measured no slower than the Y-only build on steps without an activation.
 constexpr int kEpiY = 0, kEpiAct = 1, kEpiAny = 2;
 
 // Final values of tile row n (this lane) for all rows of X: fp32 Y, or, for
 // the fused gate/up projection, the activation: rows 2j and 2j + 1 (gate and
-// up of feature j) are neighbouring lanes, and the even lane stores
-// bf16(silu(gate) * up) at column j of the bf16 [M][N/2] output.
+// up of feature j) are neighbouring lanes, which store bf16(silu(gate) * up)
+// at column j of the bf16 [M][N/2] output.
 template <int EPI>
 __device__ __forceinline__ void store_final(const ProjView& v, int n, const float (&val)[kN],
                                             int lane) {
@@ -584,15 +586,26 @@ __device__ __forceinline__ void store_final(const ProjView& v, int n, const floa
         return;
     }
     if constexpr (EPI != kEpiY) {
+        // Lane pair (2i, 2i+1) holds rows 2i (gate) and 2i+1 (up) of activation
+        // column i.  Both lanes swap their values and split the batch rows: the
+        // even lane takes rows 0, 2, 4, ..., the odd lane rows 1, 3, 5, ...  The
+        // fast exponential and division keep this path short; their relative
+        // error (a few fp32 ulps) is far below the bf16 rounding step.  Where
+        // 1 + exp(-g) exceeds 2^126 (gate below about -87.3) the quotient
+        // comes out as zero instead of a value under 1e-36 times abs(up).
         __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(v.y);
         const int nf = v.N >> 1, f = n >> 1;
-        const bool even = (lane & 1) == 0 && n < v.N;
+        const bool odd = (lane & 1) != 0;
+        const bool live = n < v.N;
 #pragma unroll
-        for (int j = 0; j < kN; ++j) {
-            const float g = val[j];
-            const float u = __shfl_xor_sync(kFull, g, 1);
-            if (even && j < v.M)
-                out[static_cast<size_t>(j) * nf + f] = __float2bfloat16_rn(g / (1.0f + expf(-g)) * u);
+        for (int jj = 0; jj < kN / 2; ++jj) {
+            const float a = val[2 * jj], b = val[2 * jj + 1];
+            const float oa = __shfl_xor_sync(kFull, a, 1), ob = __shfl_xor_sync(kFull, b, 1);
+            const float g = odd ? ob : a, u = odd ? b : oa;
+            const int j = 2 * jj + (odd ? 1 : 0);
+            if (live && j < v.M)
+                out[static_cast<size_t>(j) * nf + f] =
+                    __float2bfloat16_rn(__fdividef(g, 1.0f + __expf(-g)) * u);
         }
     }
 }
@@ -1289,9 +1302,9 @@ cudaError_t launch_tc(const CUtensorMap& tmW, const CUtensorMap& tmX, const Gemm
 // Fused step launch; cooperative (all CTAs resident at once) when projections
 // wait for one another.
 template <int BITS, int G>
-cudaError_t launch_step(const StepArgs& sa, bool cooperative, bool any_act, cudaStream_t s) {
+cudaError_t launch_step(const StepArgs& sa, bool cooperative, cudaStream_t s) {
     using L = Lay<BITS, G>;
-    auto kern = any_act ? gemm_tc_kernel<BITS, G, true, kEpiAny> : gemm_tc_kernel<BITS, G, true, kEpiY>;
+    auto kern = gemm_tc_kernel<BITS, G, true, kEpiAny>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
     if (e != cudaSuccess) return e;

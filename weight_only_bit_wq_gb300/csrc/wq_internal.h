@@ -102,14 +102,10 @@ cudaError_t launch_gemm_tc_b3(int group, const CUtensorMap& tmW, const CUtensorM
 cudaError_t launch_gemm_tc_b2(int group, const CUtensorMap& tmW, const CUtensorMap& tmX,
                               const GemmArgs& a, cudaStream_t s);
 // Fused step: all projections of `sa` (one bit width and group size) in one
-// persistent launch; cooperative when any projection waits for another;
-// any_act: some projection has the fused gate/up activation epilogue.
-cudaError_t launch_step_b4(int group, const StepArgs& sa, bool cooperative, bool any_act,
-                           cudaStream_t s);
-cudaError_t launch_step_b3(int group, const StepArgs& sa, bool cooperative, bool any_act,
-                           cudaStream_t s);
-cudaError_t launch_step_b2(int group, const StepArgs& sa, bool cooperative, bool any_act,
-                           cudaStream_t s);
+// persistent launch; cooperative when any projection waits for another.
+cudaError_t launch_step_b4(int group, const StepArgs& sa, bool cooperative, cudaStream_t s);
+cudaError_t launch_step_b3(int group, const StepArgs& sa, bool cooperative, cudaStream_t s);
+cudaError_t launch_step_b2(int group, const StepArgs& sa, bool cooperative, cudaStream_t s);
 
 // wq_gemm with the launch mode chosen by the caller: pdl = launch as a
 // programmatic dependent of the previous kernel on the stream (only where

@@ -157,8 +157,7 @@ wq_status_t build_table(const wq_proj_desc_t* projs, const Run& r, std::vector<w
 
 // Reset the run's completion counters and launch its persistent kernel.
 wq_status_t launch_run(const Run& r, Tables tab, int nphase, long long units, bool waits,
-                       bool any_act, uint8_t* ws, const FusedLayout& lay, int sms,
-                       cudaStream_t s) {
+                       uint8_t* ws, const FusedLayout& lay, int sms, cudaStream_t s) {
     const int n = r.end - r.begin;
     int* done = reinterpret_cast<int*>(ws + lay.done_off);
     cudaError_t e = cudaMemsetAsync(done, 0, static_cast<size_t>(n) * sizeof(int), s);
@@ -175,11 +174,11 @@ wq_status_t launch_run(const Run& r, Tables tab, int nphase, long long units, bo
     sa.U = units;
     sa.P = static_cast<int>(std::min<long long>(sms, units));
     if (r.bits == 4)
-        e = wq::launch_step_b4(r.group, sa, waits, any_act, s);
+        e = wq::launch_step_b4(r.group, sa, waits, s);
     else if (r.bits == 3)
-        e = wq::launch_step_b3(r.group, sa, waits, any_act, s);
+        e = wq::launch_step_b3(r.group, sa, waits, s);
     else
-        e = wq::launch_step_b2(r.group, sa, waits, any_act, s);
+        e = wq::launch_step_b2(r.group, sa, waits, s);
     return e == cudaSuccess ? WQ_OK : wq::host_cuda_fail(e);
 }
 
@@ -261,10 +260,8 @@ wq_status_t run_fused(const wq_proj_desc_t* projs, int count, void* workspace,
                                     phases.size() * sizeof(wq::PhaseDev), cudaMemcpyHostToDevice, s);
             if (e != cudaSuccess) return wq::host_cuda_fail(e);
         }
-        bool any_act = false;
-        for (int i = r.begin; i < r.end; ++i) any_act = any_act || projs[i].epilogue != WQ_EPI_NONE;
         if (wq_status_t st = launch_run(r, tab, static_cast<int>(phases.size()), units, waits,
-                                        any_act, ws, lay, sms, s))
+                                        ws, lay, sms, s))
             return st;
     }
     return WQ_OK;
