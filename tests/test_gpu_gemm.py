@@ -101,6 +101,22 @@ def test_config_full_size_sampled_rows(name):
     assert np.isfinite(y).all()
 
 
+def test_fused_qkv_projection_sampled_rows():
+    # q, k and v of one layer concatenated along N (5120 + 1024 + 1024 rows)
+    # stream as one projection; sampled rows against the oracle
+    p = synth.Projection("qkv", 12, 7168, 5120, 4, 128, 11)
+    wqw, s, z = _device_weights(p)
+    x = synth.gen_x(p)
+    xd = torch.from_numpy(x.view(np.int16)).to(dev())
+    y = _wq().wq_gemm(xd, wqw, s, z, p.N, p.group, p.bits).cpu().numpy()
+    rows = _sample_rows(p.N)
+    rows = np.unique(np.concatenate([rows, [5119, 5120, 6143, 6144]]))
+    ws = synth.gen_weights(p, rows=rows)
+    y_ref = oracle.gemm_f64(x, oracle.pack(ws["q"], p.bits), ws["s"], ws["z"], p.K, p.group, p.bits)
+    err = rel_err(y[:, rows], y_ref)
+    assert err <= REL_TOL and err <= ARITH_TOL, err
+
+
 def test_c3_row_subsets_bitwise():
     # rows of the 12-row call equal the same rows computed in 1-, 5- and 9-row calls
     p = synth.CONFIGS["C3"]
