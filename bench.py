@@ -39,6 +39,7 @@ if ROOT not in sys.path:
 
 METRIC = "weight-only 4-bit GEMM weight-stream GB/s (decode step, 64 layers x 6 projections)"
 HEADLINE_M = 16
+MAX_M = 32  # widest row stack of the sweep
 L2_BYTES_FALLBACK = 129 * 2 ** 20
 
 
@@ -249,16 +250,16 @@ class StepStack:
 
         self.wq = wq
         self.device = device
-        self.projs = synth.step_projections(HEADLINE_M if HEADLINE_M >= 16 else 16, layers)
+        self.projs = synth.step_projections(MAX_M, layers)
         self.weights = []
         for p in self.projs:
             q, s, z = synth.gen_weights_torch(p, device)
             self.weights.append((wq.wq_pack(q, p.bits), s, z))
             del q
         torch.cuda.synchronize()
-        # activations for up to 16 rows per projection (row m never depends on M)
-        self.x16 = [synth.gen_x(p) for p in self.projs]
-        self.ws = wq.new_workspace(16, 34816, 17408, 128, 4, device=device)
+        # activations for up to MAX_M rows per projection (row m never depends on M)
+        self.xs = [synth.gen_x(p) for p in self.projs]
+        self.ws = wq.new_workspace(MAX_M, 34816, 17408, 128, 4, device=device)
         self.after = layer_dependencies(len(self.projs))
         self.ws_fused = None  # sized from the first fused descriptor set (independent of M)
 
@@ -273,7 +274,7 @@ class StepStack:
         import numpy as np
         import torch
 
-        xs = [np.ascontiguousarray(x[:M]).reshape(-1) for x in self.x16]
+        xs = [np.ascontiguousarray(x[:M]).reshape(-1) for x in self.xs]
         x_host = torch.from_numpy(np.concatenate(xs).view(np.int16)).pin_memory()
         x_dev = x_host.to(self.device)
         ny = sum(M * p.N for p in self.projs)
@@ -522,6 +523,8 @@ def main_ours(args):
     peak, peak_kind = load_peaks()
     l2 = getattr(torch.cuda.get_device_properties(device), "L2_cache_size", L2_BYTES_FALLBACK)
     stream = torch.cuda.Stream(device)
+    import synth
+
     stack = StepStack(args.layers, device)
     clocks = ClockSampler(_gpu_id(device)) if rank == 0 else None
 
@@ -533,7 +536,7 @@ def main_ours(args):
 
     sweep = []
     if not args.no_sweep:
-        for M in (1, 2, 4, 8, 12, 16):
+        for M in synth.STEP_M_SWEEP:
             r = run_sweep_point(stack, M, stream, max(3, args.steps // 4), 2, dist)
             b = stack.step_bytes(M)
             ms = reduce_max(dist, r["ms_per_step"], device)

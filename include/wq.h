@@ -6,7 +6,7 @@
  * from memory once and, while on chip, multiplied against all stacked rows
  * (each active agent's next token plus its draft tokens):
  *
- *     Y[M][N] = X[M][K] . dequant(Wq)[N][K]^T,   M = 1..16
+ *     Y[M][N] = X[M][K] . dequant(Wq)[N][K]^T,   M = 1..32
  *     dequant(Wq)[n][k] = (q[n][k] - z[n][k/G]) * s[n][k/G]
  *
  * with 2/3/4-bit codes chosen per layer and repacked at load time (Agens
@@ -18,13 +18,16 @@
  * caller unless stated otherwise):
  *   q       uint8  [N][K]        unpacked codes; only the low `bits` bits are used
  *   wq      uint32 [N][W]        packed codes, W = wq_packed_words_per_row(K, bits):
- *                                code k of a row lives in word k / vpw at bits
- *                                [bits*(k % vpw), bits*(k % vpw) + bits), least
- *                                significant first; vpw = 8 (4-bit), 10 (3-bit,
- *                                bits 30..31 zero), 16 (2-bit); words run along K
- *                                across group boundaries; unused slots and the
- *                                padding words that round a row up to a multiple
- *                                of 4 words (16 bytes) are zero
+ *                                code k of a row lives in word k / vpw; with
+ *                                j = k % vpw it takes bits [16*(j % 2) +
+ *                                bits*(j / 2), ... + bits): even-numbered codes
+ *                                fill the low half-word and odd-numbered codes
+ *                                the high half-word, each half least significant
+ *                                first; vpw = 8 (4-bit), 10 (3-bit, bits 15 and
+ *                                31 zero), 16 (2-bit); words run along K across
+ *                                group boundaries; unused slots and the padding
+ *                                words that round a row up to a multiple of 4
+ *                                words (16 bytes) are zero
  *   scales  bf16   [N][K/G]      per-group scale s (bf16 bit patterns, uint16)
  *   zeros   uint8  [N][K/G]      per-group zero point z
  *   x       bf16   [M][K]        activations (bf16 bit patterns)
@@ -32,7 +35,9 @@
  *   w       bf16   [N][K]        dequantised weights (wq_dequant output)
  *
  * Arguments: bits in {2, 3, 4}; group in {32, 64, 128}; K % group == 0;
- * 0 <= M <= 16; N, K >= 0.  x and wq must be 16-byte aligned, y 4-byte
+ * 0 <= M <= 32 (up to 16 rows per MMA column block: M <= 16 runs the 16-row
+ * kernel build, 17..32 the 32-row build, and a row's result is bitwise the
+ * same in both); N, K >= 0.  x and wq must be 16-byte aligned, y 4-byte
  * aligned, scales 2-byte aligned (16-byte aligned scales and zeros take a
  * faster path in wq_gemm).  Streams are passed as `void*` holding a
  * cudaStream_t (NULL = the legacy default stream).  Every call is
@@ -134,8 +139,10 @@ wq_status_t wq_gemm(const uint16_t* x, const uint32_t* wq, const uint16_t* scale
 /*
  * wq_gemm_swiglu — the fused gate/up projection of a gated MLP with its
  * activation applied in the epilogue: y[m][j] = RNE_bf16(silu(g) * u) with
- * g = acc[m][2j], u = acc[m][2j+1], silu(g) = g / (1 + e^-g) in fp32, acc the
- * wq_gemm sums.  The pages fuse gate and up into one weight stream (OpenJet
+ * g = acc[m][2j], u = acc[m][2j+1], silu(g) = g / (1 + e^-g) in fp32 with the
+ * fast exponential and division (a few fp32 ulps, far below the bf16 step; a
+ * gate below about -87.3 gives 0 where the exact value is under 1e-36 |u|),
+ * acc the wq_gemm sums.  The pages fuse gate and up into one weight stream (OpenJet
  * news page, "并行解码的原理": one pass over every weight per step) for
  * Qwen-family models without naming the activation; SwiGLU is the reading.
  * Layout: N even; weight rows (and their scale and zero-point rows) are
@@ -143,7 +150,7 @@ wq_status_t wq_gemm(const uint16_t* x, const uint32_t* wq, const uint16_t* scale
  * row; y is bf16 [M][N/2] row-major (the down projection's X), 2-byte
  * aligned.  Everything else (x, wq, scales, zeros, workspace, errors) as
  * wq_gemm; the fp32 sums are those of wq_gemm bit for bit, so y equals the
- * activation applied to wq_gemm's output up to the last bit of expf.
+ * activation applied to wq_gemm's output to within one bf16 step.
  */
 wq_status_t wq_gemm_swiglu(const uint16_t* x, const uint32_t* wq, const uint16_t* scales,
                            const uint8_t* zeros, uint16_t* y, int M, int N, int K, int group,

@@ -172,7 +172,7 @@ STEP_LAYERS = 64
 STEP_PROJ = (("q", 5120, 5120), ("k", 5120, 1024), ("v", 5120, 1024),
              ("o", 5120, 5120), ("gate_up", 5120, 34816), ("down", 17408, 5120))
 STEP_SEED = 7
-STEP_M_SWEEP = (1, 2, 4, 8, 12, 16)
+STEP_M_SWEEP = (1, 2, 4, 8, 12, 16, 24, 32)
 
 
 def step_projections(M: int, layers: int = STEP_LAYERS) -> List[Projection]:

@@ -34,7 +34,7 @@ def test_every_declared_symbol_is_exported(wq):
 
 
 def test_abi_version_and_words(wq):
-    assert wq.abi_version() == 102
+    assert wq.abi_version() == 103
     assert wq.wq_packed_words_per_row(17408, 3) == 1744
     assert wq.wq_packed_words_per_row(5120, 4) == 640
     assert wq.wq_packed_words_per_row(17408, 2) == 1088
@@ -53,7 +53,7 @@ def test_gemm_rejects_bad_arguments_on_host(wq):
     assert _gemm(lib, bits=1) == bad
     assert _gemm(lib, group=96) == bad
     assert _gemm(lib, K=100, group=32) == bad     # K % group != 0
-    assert _gemm(lib, M=17) == bad
+    assert _gemm(lib, M=33) == bad
     assert _gemm(lib, M=-1) == bad
     assert _gemm(lib, N=-3) == bad
     assert _gemm(lib, y=0) == bad                 # null output

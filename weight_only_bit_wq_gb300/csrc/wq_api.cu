@@ -103,7 +103,7 @@ int choose_grid(int T, int I, int sm_count) {
 
 extern "C" {
 
-int wq_abi_version(void) { return 102; }
+int wq_abi_version(void) { return 103; }
 
 const char* wq_status_string(wq_status_t s) {
     switch (s) {
@@ -189,13 +189,13 @@ wq_status_t wq_workspace_init(void* workspace, size_t bytes, void* stream) {
 namespace {
 
 // X as one 3-D box per stage: dims {64 values, M rows, K/64 chunks}, the
-// chunk stride 128 bytes, so a box of {64, 16, c} lands in shared memory as c
-// consecutive [16 rows][128 bytes] swizzled tiles.  Requires K % 64 == 0 (a
+// chunk stride 128 bytes, so a box of {64, nc, c} lands in shared memory as c
+// consecutive [nc rows][128 bytes] swizzled tiles.  Requires K % 64 == 0 (a
 // partial chunk would alias the next row instead of reading zeros).
-wq_status_t encode_x3d(const uint16_t* x, int M, int K, int chunks, CUtensorMap* tmX) {
+wq_status_t encode_x3d(const uint16_t* x, int M, int K, int chunks, int nc, CUtensorMap* tmX) {
     const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(M), static_cast<cuuint64_t>(K / 64)};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * 2, 128};
-    const cuuint32_t box[3] = {64, 16, static_cast<cuuint32_t>(chunks)};
+    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(nc), static_cast<cuuint32_t>(chunks)};
     const cuuint32_t es[3] = {1, 1, 1};
     CUresult r = g_encode(tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(x), dims,
                           strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -204,7 +204,7 @@ wq_status_t encode_x3d(const uint16_t* x, int M, int K, int chunks, CUtensorMap*
 }
 
 wq_status_t encode_maps(const uint16_t* x, const uint32_t* wq, int M, int N, int K, int W,
-                        CUtensorMap* tmW, CUtensorMap* tmX) {
+                        int nc, CUtensorMap* tmW, CUtensorMap* tmX) {
     if (wq_status_t st = get_encoder()) return st;
     {
         const cuuint64_t dims[2] = {static_cast<cuuint64_t>(W), static_cast<cuuint64_t>(N)};
@@ -221,7 +221,7 @@ wq_status_t encode_maps(const uint16_t* x, const uint32_t* wq, int M, int N, int
     {
         const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
         const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
-        const cuuint32_t box[2] = {64, 16};
+        const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(nc)};
         const cuuint32_t es[2] = {1, 1};
         CUresult r = g_encode(tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(x), dims,
                               strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -283,13 +283,14 @@ wq_status_t host_check_gemm(const uint16_t* x, const uint32_t* wq, const uint16_
 
 wq_status_t host_encode_proj(const uint16_t* x, const uint32_t* wq, const uint16_t* scales,
                              const uint8_t* zeros, int M, int N, int K, int group, int bits,
-                             CUtensorMap* tmW, CUtensorMap* tmX, int* x3d, int* meta_vec) {
+                             int nc, CUtensorMap* tmW, CUtensorMap* tmX, int* x3d,
+                             int* meta_vec) {
     const int W = static_cast<int>(wq_packed_words_per_row(K, bits));
     const int sv = tc_stage_values(bits, group);
-    if (wq_status_t st = encode_maps(x, wq, M, N, K, W, tmW, tmX)) return st;
+    if (wq_status_t st = encode_maps(x, wq, M, N, K, W, nc, tmW, tmX)) return st;
     *x3d = K % 64 == 0 ? 1 : 0;
     if (*x3d)
-        if (wq_status_t st = encode_x3d(x, M, K, sv / 64, tmX)) return st;
+        if (wq_status_t st = encode_x3d(x, M, K, sv / 64, nc, tmX)) return st;
     const int ng = K / group;
     const int gps = sv / group;
     const bool gps_pow2 = (gps & (gps - 1)) == 0;
@@ -331,8 +332,9 @@ wq_status_t gemm_run(const uint16_t* x, const uint32_t* wq, const uint16_t* scal
 
     CUtensorMap tmW, tmX;
     wq::GemmArgs a;
-    if (wq_status_t st = wq::host_encode_proj(x, wq, scales, zeros, M, N, K, group, bits, &tmW,
-                                              &tmX, &a.x3d, &a.meta_vec))
+    a.nc = wq::tc_cols(M);
+    if (wq_status_t st = wq::host_encode_proj(x, wq, scales, zeros, M, N, K, group, bits, a.nc,
+                                              &tmW, &tmX, &a.x3d, &a.meta_vec))
         return st;
     a.scales = scales;
     a.zeros = zeros;

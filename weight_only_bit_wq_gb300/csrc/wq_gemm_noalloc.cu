@@ -13,8 +13,9 @@
 namespace {
 
 // Fixed scratch size.  Enough for the split-K partials of up to 2 x (SM count)
-// CTAs (2.5 MB on a 152-SM GB300) plus eight counters per 128-row tile.
-constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;
+// CTAs (5 MB on a 152-SM GB300) plus the arrival counters of about 49,000
+// 128-row tiles.
+constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 

@@ -1,5 +1,5 @@
 // Weight-only low-bit skinny GEMM on the 5th-generation tensor core (sm_103a):
-//     Y[M][N] = X[M][K] . dequant(Wq)[N][K]^T,  M <= 16, 2/3/4-bit codes.
+//     Y[M][N] = X[M][K] . dequant(Wq)[N][K]^T,  M <= 32, 2/3/4-bit codes.
 //
 // A decode-step projection streams every packed weight once and multiplies it,
 // while on chip, against all stacked rows of X on tensor cores (OpenJet news
@@ -8,8 +8,9 @@
 // count) only.  Warp roles (warp-specialised, connected by mbarrier rings):
 //
 // * TMA producer (one lane): per stage one or two 128-row x 128-byte boxes of
-//   packed words and the matching X slice (16 rows x stage width, rows >= M
-//   read as zero), all 128-byte swizzled, into a ring of shared-memory stages;
+//   packed words and the matching X slice (NC = 16 or 32 rows x stage width,
+//   rows >= M read as zero), all 128-byte swizzled, into a ring of
+//   shared-memory stages;
 // * unpack warps (two per TMEM lane quarter, each taking half of every
 //   group's K steps): one weight row per thread.  The "magic number" trick
 //   turns codes into bf16 — a code q placed in the mantissa of 128.0 reads as
@@ -18,7 +19,8 @@
 //   LOP3 produce the bf16 pair of two neighbouring codes.  The pairs go to
 //   tensor memory (tcgen05.st) as the MMA's A tile;
 // * MMA issuer (one elected lane; the warp also owns the TMEM allocation):
-//   tcgen05.mma kind::f16, M = 128 weight rows, N = 16 rows of X, K = 16,
+//   tcgen05.mma kind::f16, M = 128 weight rows, N = 16 rows of X, K = 16
+//   (two such MMAs, one per 16 rows, when the tile carries 32 rows of X),
 //   A from tensor memory, B (X) straight from the swizzled shared tile
 //   through a matrix descriptor, fp32 D per group in tensor memory.  The zero
 //   point is applied on the tensor core: a second MMA per K step multiplies
@@ -26,14 +28,16 @@
 //   row, so each group's D is sum_k x (q - z) (where tensor memory is too
 //   small for those tiles, q - z is formed on the CUDA cores instead);
 // * epilogue warps (one per lane quarter): write the zero-point tiles, read
-//   each group's D back (tcgen05.ld), add scale * D to the row's 16 fp32
+//   each group's D back (tcgen05.ld), add scale * D to the row's NC fp32
 //   sums, and store Y or publish a split-K partial.
 //
 // Tensor memory holds rings of A-tile batch slots and accumulator slots, so
 // the unpack warps run ahead of the tensor core and never wait for a result.
 // Per group the D accumulation order is fixed (data MMA then zero-point MMA
 // per K step, K steps ascending) and the columns of one MMA never interact,
-// so a row of X gives bit-identical results alone or stacked.  A tile split
+// so a row of X gives bit-identical results alone or stacked; a 32-row tile
+// issues for rows 16..31 the same N = 16 MMA as for rows 0..15, so rows agree
+// between the 16- and the 32-row builds too.  A tile split
 // across CTAs is summed by the last CTA to finish it, in k order.
 #pragma once
 #include <cuda_bf16.h>
@@ -45,9 +49,12 @@
 namespace wq {
 namespace tc {
 
-constexpr int kN = 16;  // MMA N: rows of X (M padded to 16)
+constexpr int kMmaN = 16;  // N of one MMA: 16 rows of X
 constexpr uint32_t kTmemCols = 512;
-constexpr int kSmemBudgetTc = 220 * 1024;
+// Shared memory for the stage ring: 16-row builds keep the stage counts
+// measured with this budget; 32-row builds take a little more so that every
+// format keeps three stages.
+constexpr int smem_budget_tc(int nc) { return (nc == 16 ? 220 : 226) * 1024; }
 // Unpack warps per TMEM lane quarter (each takes 1 / kSplitWarps of a
 // group's K steps): two per lane quarter measured best; more add per-warp
 // overhead without adding ALU throughput.
@@ -63,18 +70,29 @@ constexpr int clamp_tc(int v, int lo, int hi) { return v < lo ? lo : (v > hi ? h
 // Tensor-memory plan for batch slots of R groups: returns 100 z + 10 na + nd
 // for the first of (zero point on the tensor core z, na A slots, nd
 // accumulator slots) that fits, trying z = 1 before z = 0, then two
-// accumulator slots before one, then three A slots before two; 0 if none fits.
-constexpr int tmem_plan(int R, int a_cols, int n, int cols) {
-    for (int z = 1; z >= 0; --z)
+// accumulator slots before one, then three A slots before two, and a single
+// A slot only when nothing else fits; 0 if none fits.  z_only >= 0 fixes z:
+// the 32-row build keeps the 16-row build's zero-point method, whose fp32
+// rounding differs, so that rows agree bitwise between the two builds.
+constexpr int tmem_plan(int R, int a_cols, int n, int cols, int z_only = -1) {
+    for (int z = 1; z >= 0; --z) {
+        if (z_only >= 0 && z != z_only) continue;
         for (int nd = 2; nd >= 1; --nd)
             for (int na = 3; na >= 2; --na)
                 if (round_up_tc(na * R * (a_cols + 8 * z), 16) + nd * R * n <= cols)
                     return 100 * z + 10 * na + nd;
+        for (int nd = 2; nd >= 1; --nd)
+            if (round_up_tc(R * (a_cols + 8 * z), 16) + nd * R * n <= cols)
+                return 100 * z + 10 + nd;
+    }
     return 0;
 }
 
-template <int BITS, int G>
+// Layout of a build for BITS-bit codes, group size G and NC rows of X per
+// tile (16 for M <= 16, 32 for M <= 32).
+template <int BITS, int G, int NC = 16>
 struct Lay {
+    static_assert(NC == 16 || NC == 32, "16 or 32 rows of X");
     static constexpr int kVpw = values_per_word(BITS);
     static constexpr int kPpw = kVpw / 2;                    // bf16 pairs per word
     static constexpr int kBoxes = tc_boxes(BITS, G);         // 32-word boxes per row per stage
@@ -86,7 +104,7 @@ struct Lay {
     static constexpr int kWBytes = kBoxes * kBoxBytes;
     static constexpr int kXBoxValues = 64;                      // 128 bytes of bf16
     static constexpr int kXBoxes = kStageValues / kXBoxValues;
-    static constexpr int kXBoxBytes = kN * 128;                 // 16 rows x 128 bytes
+    static constexpr int kXBoxBytes = NC * 128;                 // NC rows x 128 bytes
     static constexpr int kXBytes = kXBoxes * kXBoxBytes;
     static constexpr int kGPS = kStageValues / G;               // groups per stage
     // The stage also carries its rows' zero points, kZRow bytes per row (kGPS
@@ -113,21 +131,23 @@ struct Lay {
     // A stage's groups go through the tensor core in two batches, [0, kR0)
     // and [kR0, kGPS); a batch slot in tensor memory holds kR0 groups.
     static constexpr int kR0 = (kGPS + 1) / 2;
-    static constexpr int kStages = clamp_tc(kSmemBudgetTc / kStageBytes, 2, 8);
+    static constexpr int kStages = clamp_tc(smem_budget_tc(NC) / kStageBytes, 2, 8);
     static constexpr int kBarOffset = kStages * kStageBytes;
     static constexpr int kSmemBytes = kBarOffset + 512 + 1024;  // barriers/flags + align slack
     // Tensor memory: kNA batch slots of A tiles (plus zero-point tiles when
     // the zero point goes on the tensor core) and kND batch slots of fp32
     // accumulators, the largest plan that fits in 512 columns.
-    static constexpr int kPlan = tmem_plan(kR0, kACols, kN, int(kTmemCols));
+    static constexpr int kPlan16 = tmem_plan(kR0, kACols, 16, int(kTmemCols));
+    static constexpr int kPlan =
+        NC == 16 ? kPlan16 : tmem_plan(kR0, kACols, NC, int(kTmemCols), kPlan16 / 100);
     static constexpr bool kZtc = kPlan / 100 != 0;
     static constexpr int kNA = (kPlan / 10) % 10;
     static constexpr int kND = kPlan % 10;
     static constexpr uint32_t kColA = 0;                                        // [kNA][kR0][kACols]
     static constexpr uint32_t kColZ = kNA * kR0 * kACols;                       // [kNA][kR0][8]
-    static constexpr uint32_t kColD = round_up_tc(kColZ + (kZtc ? kNA * kR0 * 8 : 0), 16);  // [kND][kR0][16]
+    static constexpr uint32_t kColD = round_up_tc(kColZ + (kZtc ? kNA * kR0 * 8 : 0), 16);  // [kND][kR0][NC]
     static_assert(kPlan > 0, "no tensor-memory plan fits");
-    static_assert(kColD + kND * kR0 * kN <= kTmemCols, "tensor memory budget");
+    static_assert(kColD + kND * kR0 * NC <= kTmemCols, "tensor memory budget");
     static_assert(kPairsW == 8 || kPairsW == 16 || kPairsW == 32, "tcgen05.st width");
     static_assert(kEW <= kCountersPerTile, "one split-K counter per epilogue warp");
     static_assert(kR0 >= 1 && kGPS - kR0 >= 1, "two non-empty batches");
@@ -136,7 +156,7 @@ struct Lay {
 // Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B bf16
 // (bits 7-9 = 1, bits 10-12 = 1), both K-major (bits 15, 16 = 0),
 // N >> 3 in bits 17-22, M >> 4 in bits 24-28.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(kN >> 3) << 17) |
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(kMmaN >> 3) << 17) |
                             (uint32_t(128 >> 4) << 24);
 
 // Shared-memory matrix descriptor of a K-major operand stored with the 128-byte
@@ -331,10 +351,10 @@ __device__ __forceinline__ void static_for(F&& f) {
 //   row_sw: shared address of the row inside the stage, with the row's
 //           swizzle pattern (row % 8) << 4 already XOR-ed in;
 //   tA:     TMEM address of the group's A tile in the warp's lane quarter.
-template <int BITS, int G, int H, int GI>
+template <int BITS, int G, int NC, int H, int GI>
 __device__ __forceinline__ void write_group(uint32_t row_sw, uint32_t tA,
                                             const RowMeta<Lay<BITS, G>::kGPS>& m) {
-    using L = Lay<BITS, G>;
+    using L = Lay<BITS, G, NC>;
     using P = WordPlan<BITS, G, H, GI>;
     uint32_t w[P::kNW];
     if constexpr (P::kPair) {
@@ -379,10 +399,10 @@ __device__ __forceinline__ void write_group(uint32_t row_sw, uint32_t tA,
 // The same for 2- and 4-bit codes with the K part h known only at run time:
 // each part covers a whole number of words, so all parts share one word
 // pattern and one copy of the code.
-template <int BITS, int G, int GI>
+template <int BITS, int G, int NC, int GI>
 __device__ __forceinline__ void write_group_rt(uint32_t row_sw, uint32_t tA,
                                                const RowMeta<Lay<BITS, G>::kGPS>& m, int h) {
-    using L = Lay<BITS, G>;
+    using L = Lay<BITS, G, NC>;
     constexpr int kWG = (G / 2) / L::kPpw;     // words per group
     constexpr int kWW = L::kPairsW / L::kPpw;  // words per K part
     static_assert(kWG * L::kPpw == G / 2 && kWW * L::kPpw == L::kPairsW, "whole words per part");
@@ -575,13 +595,13 @@ constexpr int kEpiY = 0, kEpiAct = 1, kEpiAny = 2;
 // the fused gate/up projection, the activation: rows 2j and 2j + 1 (gate and
 // up of feature j) are neighbouring lanes, which store bf16(silu(gate) * up)
 // at column j of the bf16 [M][N/2] output.
-template <int EPI>
-__device__ __forceinline__ void store_final(const ProjView& v, int n, const float (&val)[kN],
+template <int EPI, int NC>
+__device__ __forceinline__ void store_final(const ProjView& v, int n, const float (&val)[NC],
                                             int lane) {
     if (EPI == kEpiY || (EPI == kEpiAny && v.epi == WQ_EPI_NONE)) {
         if (n < v.N)
 #pragma unroll
-            for (int j = 0; j < kN; ++j)
+            for (int j = 0; j < NC; ++j)
                 if (j < v.M) v.y[static_cast<size_t>(j) * v.N + n] = val[j];
         return;
     }
@@ -598,7 +618,7 @@ __device__ __forceinline__ void store_final(const ProjView& v, int n, const floa
         const bool odd = (lane & 1) != 0;
         const bool live = n < v.N;
 #pragma unroll
-        for (int jj = 0; jj < kN / 2; ++jj) {
+        for (int jj = 0; jj < NC / 2; ++jj) {
             const float a = val[2 * jj], b = val[2 * jj + 1];
             const float oa = __shfl_xor_sync(kFull, a, 1), ob = __shfl_xor_sync(kFull, b, 1);
             const float g = odd ? ob : a, u = odd ? b : oa;
@@ -621,9 +641,9 @@ __device__ __forceinline__ void store_final(const ProjView& v, int n, const floa
 //   of their shares, so they have usually all arrived already.  Then the
 //   warp checks the counter first and, if they have, sums at once without
 //   publishing its own partial (two round trips fewer at the end of a share).
-template <int EPI>
+template <int EPI, int NC>
 __device__ __forceinline__ void finish_rows(const Ctx& c, const ProjView& v,
-                                            const float (&acc)[kN], int t, bool whole,
+                                            float (&acc)[NC], int t, bool whole,
                                             bool likely_last, int r, int q, int lane) {
     const int n = t * kBN + r;
     const int gt = v.toff + t;
@@ -634,7 +654,7 @@ __device__ __forceinline__ void finish_rows(const Ctx& c, const ProjView& v,
         }
     };
     if (whole) {
-        store_final<EPI>(v, n, acc, lane);
+        store_final<EPI, NC>(v, n, acc, lane);
         count_done();
         return;
     }
@@ -654,11 +674,13 @@ __device__ __forceinline__ void finish_rows(const Ctx& c, const ProjView& v,
         if (lane == 0) cnt = ld_acquire_gpu(ctr);
         last = __shfl_sync(kFull, cnt, 0) == b_last - b_first ? 1 : 0;  // all others arrived
     }
+    bool published = false;
     if (!last) {
+        published = true;
         const int own_role = c.sub_lo(v.phase, blockIdx.x) < tu0 ? 1 : 0;
         float* mine = c.partials + static_cast<size_t>(2 * blockIdx.x + own_role) * (kMaxCols * kBN);
 #pragma unroll
-        for (int j = 0; j < kN; ++j)
+        for (int j = 0; j < NC; ++j)
             if (j < v.M) __stcg(mine + j * kBN + r, acc[j]);
         // The warp barrier orders every lane's partial before lane 0's release
         // (acq_rel) increment; the reading warp's lane 0 acquires it and the
@@ -668,27 +690,56 @@ __device__ __forceinline__ void finish_rows(const Ctx& c, const ProjView& v,
         if (!__shfl_sync(kFull, last, 0)) return;
     }
     __syncwarp();  // the other lanes' reads follow lane 0's acquire
-    // all contributors in k order (this warp's own sums in place of its partial)
-    float tot[kN];
+    if constexpr (NC == 16) {
+        // all contributors in k order (this warp's own sums in place of its partial)
+        float tot[NC];
 #pragma unroll
-    for (int j = 0; j < kN; ++j) tot[j] = 0.f;
-    for (int b = b_first; b <= b_last; ++b) {
-        if (b == me) {
+        for (int j = 0; j < NC; ++j) tot[j] = 0.f;
+        for (int b = b_first; b <= b_last; ++b) {
+            if (b == me) {
 #pragma unroll
-            for (int j = 0; j < kN; ++j) tot[j] += acc[j];
+                for (int j = 0; j < NC; ++j) tot[j] += acc[j];
+            } else {
+                const float* src = c.partials +
+                                   static_cast<size_t>(2 * b + (b == b_first ? first_role : 0)) *
+                                       (kMaxCols * kBN) +
+                                   r;
+                float part[NC];
+#pragma unroll
+                for (int j = 0; j < NC; ++j) part[j] = j < v.M ? __ldcg(src + j * kBN) : 0.f;
+#pragma unroll
+                for (int j = 0; j < NC; ++j) tot[j] += part[j];
+            }
+        }
+        store_final<EPI, NC>(v, n, tot, lane);
+    } else {
+        // 32 rows: the same k-ordered sum in acc's registers, so that all 32
+        // rows of a contributor's partial load at once.  A warp that found
+        // every other contributor arrived holds the tile's first units and
+        // starts the sum with its own acc; a warp that published reads its
+        // own partial back with the others'.
+        int b = b_first;
+        if (published) {
+#pragma unroll
+            for (int j = 0; j < NC; ++j) acc[j] = 0.f;
         } else {
+#pragma unroll
+            for (int j = 0; j < NC; ++j) acc[j] = 0.f + acc[j];
+            ++b;
+        }
+        for (; b <= b_last; ++b) {
             const float* src = c.partials +
                                static_cast<size_t>(2 * b + (b == b_first ? first_role : 0)) *
                                    (kMaxCols * kBN) +
                                r;
-            float part[kN];
+            float part[NC];
 #pragma unroll
-            for (int j = 0; j < kN; ++j) part[j] = j < v.M ? __ldcg(src + j * kBN) : 0.f;
+            for (int j = 0; j < NC; ++j) part[j] = j < v.M ? __ldcg(src + j * kBN) : 0.f;
 #pragma unroll
-            for (int j = 0; j < kN; ++j) tot[j] += part[j];
+            for (int j = 0; j < NC; ++j) acc[j] += part[j];
         }
+        store_final<EPI, NC>(v, n, acc, lane);
     }
-    store_final<EPI>(v, n, tot, lane);
     if (lane == 0) *ctr = 0;
     count_done();
 }
@@ -723,11 +774,11 @@ struct Ring {
 
 // Unpack warp: turns the stage's packed words into A tiles, batch by batch.
 // HT is the warp's K part when fixed at compile time, -1 when read at run time.
-template <int BITS, int G, int HT, class B>
+template <int BITS, int G, int NC, int HT, class B>
 __device__ __forceinline__ void unpack_warp(const Ctx& c, uint32_t smem_u32, B& bars,
                                             uint32_t tmem, volatile int* abort_flag, int warp,
                                             int lane, int n_units) {
-    using L = Lay<BITS, G>;
+    using L = Lay<BITS, G, NC>;
     using RM = RowMeta<L::kGPS>;
     const int h = HT >= 0 ? HT : (warp >> 2);
     const int q = warp & 3;
@@ -766,24 +817,29 @@ __device__ __forceinline__ void unpack_warp(const Ctx& c, uint32_t smem_u32, B& 
         }
         // Both A slots of this stage must have left the tensor core: the MMAs
         // complete in order, so waiting for the later slot's previous batch
-        // covers the earlier one.
-        Ring<L::kNA> as1 = as;
-        as1.next();
-        if (!dead && !wait_all(&bars.afree[as1.slot], as1.phase ^ 1u, abort_flag)) fail();
+        // covers the earlier one.  (With a single A slot each batch waits for
+        // the one before it instead.)
+        if constexpr (L::kNA >= 2) {
+            Ring<L::kNA> as1 = as;
+            as1.next();
+            if (!dead && !wait_all(&bars.afree[as1.slot], as1.phase ^ 1u, abort_flag)) fail();
+        }
         const uint32_t row_sw = smem_u32 + st.slot * L::kStageBytes + row_off;
         static_for<0, 2>([&](auto bc) {
             constexpr int BB = decltype(bc)::value;
             constexpr int g_lo = BB == 0 ? 0 : L::kR0;
             constexpr int g_hi = BB == 0 ? L::kR0 : L::kGPS;
+            if constexpr (L::kNA == 1)
+                if (!dead && !wait_all(&bars.afree[as.slot], as.phase ^ 1u, abort_flag)) fail();
             if (!dead) {
                 const uint32_t slot_col = as.slot * (L::kR0 * L::kACols);
                 static_for<g_lo, g_hi>([&](auto gc) {
                     constexpr int GI = decltype(gc)::value;
                     const uint32_t tA = tl + L::kColA + slot_col + (GI - g_lo) * L::kACols;
                     if constexpr (HT >= 0)
-                        write_group<BITS, G, HT, GI>(row_sw, tA, cur);
+                        write_group<BITS, G, NC, HT, GI>(row_sw, tA, cur);
                     else
-                        write_group_rt<BITS, G, GI>(row_sw, tA, cur, h);
+                        write_group_rt<BITS, G, NC, GI>(row_sw, tA, cur, h);
                     // the group's zero-point tile, from one of the lane quarter's warps
                     if constexpr (L::kZtc)
                         if (GI % L::kSplit == h)
@@ -804,20 +860,20 @@ __device__ __forceinline__ void unpack_warp(const Ctx& c, uint32_t smem_u32, B& 
 }
 
 // Epilogue warp (lane quarter q).  Per unit it reads the unit's two batches
-// of accumulators back (adding scale * D to the row's 16 fp32 sums) and ends
+// of accumulators back (adding scale * D to the row's NC fp32 sums) and ends
 // tile segments.
-template <int BITS, int G, int EPI, class B>
+template <int BITS, int G, int NC, int EPI, class B>
 __device__ __forceinline__ void epilogue_warp(const Ctx& c, B& bars, uint32_t tmem,
                                               volatile int* abort_flag, int q, int lane,
                                               int n_units) {
-    using L = Lay<BITS, G>;
+    using L = Lay<BITS, G, NC>;
     using RM = RowMeta<L::kGPS>;
     const int r = 32 * q + lane;
     const uint32_t tl = tmem + (static_cast<uint32_t>(32 * q) << 16);
     bool dead = false;
-    float acc[kN];
+    float acc[NC];
 #pragma unroll
-    for (int j = 0; j < kN; ++j) acc[j] = 0.f;
+    for (int j = 0; j < NC; ++j) acc[j] = 0.f;
     auto fail = [&]() {
         record_error_tc(c.err, abort_flag);
         dead = true;
@@ -839,22 +895,40 @@ __device__ __forceinline__ void epilogue_warp(const Ctx& c, B& bars, uint32_t tm
         if (!dead && !wait_all(&bars.dfull[ds.slot], ds.phase, abort_flag)) fail();
         if (!dead) {
             tc_fence_after();
-            // two groups' accumulators at a time keep the registers in bounds
-            static_for<0, (g_hi - g_lo + 1) / 2>([&](auto pc) {
-                constexpr int G0 = g_lo + 2 * decltype(pc)::value;
-                constexpr int NG = (G0 + 1 < g_hi) ? 2 : 1;
-                uint32_t v[NG][kN];
-                static_for<0, NG>([&](auto gc) {
-                    constexpr int J = decltype(gc)::value;
-                    tmem_ld16(tl + L::kColD + (ds.slot * L::kR0 + (G0 + J - g_lo)) * kN, v[J]);
-                });
-                tmem_wait_ld();
-                static_for<0, NG>([&](auto gc) {
-                    constexpr int J = decltype(gc)::value;
-                    const float sc = m.scale(G0 + J);
+            // 32 accumulator columns in flight at most (two groups of 16); a
+            // 32-row build reads each group in two halves of 16 columns, which
+            // measured faster than one 32-column load (fewer live registers)
+            constexpr int kPG = NC == 16 ? 2 : 1;
+            static_for<0, (g_hi - g_lo + kPG - 1) / kPG>([&](auto pc) {
+                constexpr int G0 = g_lo + kPG * decltype(pc)::value;
+                constexpr int NG = (G0 + 1 < g_hi) ? kPG : 1;
+                if constexpr (NC == 16) {
+                    uint32_t v[NG][NC];
+                    static_for<0, NG>([&](auto gc) {
+                        constexpr int J = decltype(gc)::value;
+                        const uint32_t ta = tl + L::kColD + (ds.slot * L::kR0 + (G0 + J - g_lo)) * NC;
+                        tmem_ld16(ta, v[J]);
+                    });
+                    tmem_wait_ld();
+                    static_for<0, NG>([&](auto gc) {
+                        constexpr int J = decltype(gc)::value;
+                        const float sc = m.scale(G0 + J);
 #pragma unroll
-                    for (int j = 0; j < kN; ++j) acc[j] = fmaf(sc, __uint_as_float(v[J][j]), acc[j]);
-                });
+                        for (int j = 0; j < NC; ++j) acc[j] = fmaf(sc, __uint_as_float(v[J][j]), acc[j]);
+                    });
+                } else {
+                    const uint32_t ta = tl + L::kColD + (ds.slot * L::kR0 + (G0 - g_lo)) * NC;
+                    const float sc = m.scale(G0);
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        uint32_t v16[16];
+                        tmem_ld16(ta + 16 * hh, v16);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            acc[16 * hh + j] = fmaf(sc, __uint_as_float(v16[j]), acc[16 * hh + j]);
+                    }
+                }
             });
             tc_fence_before();
         }
@@ -877,10 +951,10 @@ __device__ __forceinline__ void epilogue_warp(const Ctx& c, B& bars, uint32_t tm
         const bool end = tile_end || cc.last_of_share();
         if (end) {
             if (!dead)
-                finish_rows<EPI>(c, cc.v, acc, cc.t, seg_from_start && tile_end,
+                finish_rows<EPI, NC>(c, cc.v, acc, cc.t, seg_from_start && tile_end,
                             seg_from_start && !tile_end, r, q, lane);
 #pragma unroll
-            for (int j = 0; j < kN; ++j) acc[j] = 0.f;
+            for (int j = 0; j < NC; ++j) acc[j] = 0.f;
         }
         cc.next(c);
         if (end) seg_from_start = cc.i == 0;
@@ -915,11 +989,11 @@ __device__ __forceinline__ bool wait_deps(const Ctx& c, int upto, int& verified,
     }
 }
 
-template <int BITS, int G, bool MULTI, int EPI>
-__global__ void __launch_bounds__(Lay<BITS, G>::kThreads, 1)
+template <int BITS, int G, int NC, bool MULTI, int EPI>
+__global__ void __launch_bounds__(Lay<BITS, G, NC>::kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                    const GemmArgs a, const StepArgs sa) {
-    using L = Lay<BITS, G>;
+    using L = Lay<BITS, G, NC>;
     constexpr int S = L::kStages;
     using BarsT = Bars<S, L::kNA, L::kND>;
     static_assert(sizeof(BarsT) <= 512, "barrier block");
@@ -1225,14 +1299,20 @@ __global__ void __launch_bounds__(Lay<BITS, G>::kThreads, 1)
                         constexpr int GI = decltype(gc)::value;
                         const uint32_t tA = tmem + L::kColA + (as.slot * L::kR0 + (GI - g_lo)) * L::kACols;
                         const uint32_t tZ = tmem + L::kColZ + (as.slot * L::kR0 + (GI - g_lo)) * 8;
-                        const uint32_t tD = tmem + L::kColD + (ds.slot * L::kR0 + (GI - g_lo)) * kN;
+                        const uint32_t tD = tmem + L::kColD + (ds.slot * L::kR0 + (GI - g_lo)) * NC;
 #pragma unroll
                         for (int s = 0; s < L::kSteps; ++s) {
                             const int v0 = GI * G + 16 * s;  // first value of this K step in the stage
                             const uint64_t bdesc =
                                 desc0 + static_cast<uint64_t>(((v0 / 64) * L::kXBoxBytes + (v0 % 64) * 2) >> 4);
-                            tc_mma_ts(tD, tA + 8 * s, bdesc, kIdesc, s > 0 ? 1u : 0u);
-                            if constexpr (L::kZtc) tc_mma_ts(tD, tZ, bdesc, kIdesc, 1u);
+                            // rows 16 h .. 16 h + 15 of X: 16 rows of 128 bytes further
+                            // into the box, accumulator columns 16 h ..
+#pragma unroll
+                            for (int hh = 0; hh < NC / kMmaN; ++hh) {
+                                const uint64_t bd = bdesc + static_cast<uint64_t>((hh * kMmaN * 128) >> 4);
+                                tc_mma_ts(tD + hh * kMmaN, tA + 8 * s, bd, kIdesc, s > 0 ? 1u : 0u);
+                                if constexpr (L::kZtc) tc_mma_ts(tD + hh * kMmaN, tZ, bd, kIdesc, 1u);
+                            }
                         }
                     });
                     tc_commit(&bars.afree[as.slot]);
@@ -1259,26 +1339,26 @@ __global__ void __launch_bounds__(Lay<BITS, G>::kThreads, 1)
 
     if (warp >= L::kUW) {
         // ------------------------------------------------------------ epilogue
-        epilogue_warp<BITS, G, EPI>(c, bars, tmem, abort_flag, warp & 3, lane, n_units);
+        epilogue_warp<BITS, G, NC, EPI>(c, bars, tmem, abort_flag, warp & 3, lane, n_units);
     } else if constexpr (BITS == 3) {
         // ------------------------------------------------------------ unpack
         static_for<0, L::kSplit>([&](auto hc) {
             constexpr int H = decltype(hc)::value;
             if ((warp >> 2) == H)
-                unpack_warp<BITS, G, H>(c, smem_u32, bars, tmem, abort_flag, warp, lane, n_units);
+                unpack_warp<BITS, G, NC, H>(c, smem_u32, bars, tmem, abort_flag, warp, lane, n_units);
         });
     } else {
-        unpack_warp<BITS, G, -1>(c, smem_u32, bars, tmem, abort_flag, warp, lane, n_units);
+        unpack_warp<BITS, G, NC, -1>(c, smem_u32, bars, tmem, abort_flag, warp, lane, n_units);
     }
     named_bar_sync(3, kTail);
 }
 
-template <int BITS, int G>
-cudaError_t launch_tc(const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmArgs& a,
-                      cudaStream_t s) {
-    using L = Lay<BITS, G>;
-    auto kern = a.epi == WQ_EPI_SWIGLU ? gemm_tc_kernel<BITS, G, false, kEpiAct>
-                                       : gemm_tc_kernel<BITS, G, false, kEpiY>;
+template <int BITS, int G, int NC>
+cudaError_t launch_tc_nc(const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmArgs& a,
+                         cudaStream_t s) {
+    using L = Lay<BITS, G, NC>;
+    auto kern = a.epi == WQ_EPI_SWIGLU ? gemm_tc_kernel<BITS, G, NC, false, kEpiAct>
+                                       : gemm_tc_kernel<BITS, G, NC, false, kEpiY>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
     if (e != cudaSuccess) return e;
@@ -1299,12 +1379,20 @@ cudaError_t launch_tc(const CUtensorMap& tmW, const CUtensorMap& tmX, const Gemm
     return cudaLaunchKernelEx(&cfg, kern, tmW, tmX, a, StepArgs{});
 }
 
+// Single projection: the 16-row build for M <= 16, the 32-row one above.
+template <int BITS, int G>
+cudaError_t launch_tc(const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmArgs& a,
+                      cudaStream_t s) {
+    return a.nc == 32 ? launch_tc_nc<BITS, G, 32>(tmW, tmX, a, s)
+                      : launch_tc_nc<BITS, G, 16>(tmW, tmX, a, s);
+}
+
 // Fused step launch; cooperative (all CTAs resident at once) when projections
 // wait for one another.
-template <int BITS, int G>
-cudaError_t launch_step(const StepArgs& sa, bool cooperative, cudaStream_t s) {
-    using L = Lay<BITS, G>;
-    auto kern = gemm_tc_kernel<BITS, G, true, kEpiAny>;
+template <int BITS, int G, int NC>
+cudaError_t launch_step_nc(const StepArgs& sa, bool cooperative, cudaStream_t s) {
+    using L = Lay<BITS, G, NC>;
+    auto kern = gemm_tc_kernel<BITS, G, NC, true, kEpiAny>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
     if (e != cudaSuccess) return e;
@@ -1321,6 +1409,12 @@ cudaError_t launch_step(const StepArgs& sa, bool cooperative, cudaStream_t s) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kern, none, none, a, sa);
+}
+
+template <int BITS, int G>
+cudaError_t launch_step(const StepArgs& sa, bool cooperative, int nc, cudaStream_t s) {
+    return nc == 32 ? launch_step_nc<BITS, G, 32>(sa, cooperative, s)
+                    : launch_step_nc<BITS, G, 16>(sa, cooperative, s);
 }
 
 }  // namespace tc

@@ -11,10 +11,10 @@ cudaError_t launch_gemm_tc_b2(int group, const CUtensorMap& tmW, const CUtensorM
     return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_step_b2(int group, const StepArgs& sa, bool cooperative, cudaStream_t s) {
-    if (group == 128) return tc::launch_step<2, 128>(sa, cooperative, s);
-    if (group == 64) return tc::launch_step<2, 64>(sa, cooperative, s);
-    if (group == 32) return tc::launch_step<2, 32>(sa, cooperative, s);
+cudaError_t launch_step_b2(int group, const StepArgs& sa, bool cooperative, int nc, cudaStream_t s) {
+    if (group == 128) return tc::launch_step<2, 128>(sa, cooperative, nc, s);
+    if (group == 64) return tc::launch_step<2, 64>(sa, cooperative, nc, s);
+    if (group == 32) return tc::launch_step<2, 32>(sa, cooperative, nc, s);
     return cudaErrorInvalidValue;
 }
 

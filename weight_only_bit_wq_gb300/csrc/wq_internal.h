@@ -11,7 +11,7 @@ namespace wq {
 
 constexpr int kBN = 128;              // weight rows per tile (TMEM lanes)
 constexpr int kWordsPerStage = 32;    // packed words per row per TMA box (128 B)
-constexpr int kMaxCols = 16;          // max stacked rows M
+constexpr int kMaxCols = 32;          // max stacked rows M
 constexpr int kMaxSplit = 8;          // max CTAs sharing one tile
 constexpr int kCountersPerTile = 16;  // split-K arrival counters per tile (one per consumer warp)
 constexpr size_t kWsHeader = 256;     // error word + padding
@@ -26,6 +26,9 @@ constexpr int tc_boxes(int bits, int group) {
 constexpr int tc_stage_values(int bits, int group) {
     return tc_boxes(bits, group) * kWordsPerStage * values_per_word(bits);
 }
+// Rows of X per tile of the kernel build that serves M rows: 16 up to 16,
+// else 32 (the 32-row build issues two 16-row MMAs per K step).
+constexpr int tc_cols(int M) { return M > 16 ? 32 : 16; }
 
 struct GemmArgs {
     const uint16_t* scales;
@@ -43,6 +46,7 @@ struct GemmArgs {
     int pdl;          // launched as a programmatic dependent of the previous kernel on the
                       // stream: X is read, and anything written, once that kernel completed
     int epi;          // WQ_EPI_NONE or WQ_EPI_SWIGLU (y is then bf16 [M][N/2])
+    int nc;           // rows of X per tile: tc_cols(M); the X map's box has nc rows
 };
 
 // One projection of a fused step, as the step kernel reads it from device
@@ -102,10 +106,14 @@ cudaError_t launch_gemm_tc_b3(int group, const CUtensorMap& tmW, const CUtensorM
 cudaError_t launch_gemm_tc_b2(int group, const CUtensorMap& tmW, const CUtensorMap& tmX,
                               const GemmArgs& a, cudaStream_t s);
 // Fused step: all projections of `sa` (one bit width and group size) in one
-// persistent launch; cooperative when any projection waits for another.
-cudaError_t launch_step_b4(int group, const StepArgs& sa, bool cooperative, cudaStream_t s);
-cudaError_t launch_step_b3(int group, const StepArgs& sa, bool cooperative, cudaStream_t s);
-cudaError_t launch_step_b2(int group, const StepArgs& sa, bool cooperative, cudaStream_t s);
+// persistent launch; cooperative when any projection waits for another; nc
+// rows of X per tile (every projection's X map has boxes of nc rows).
+cudaError_t launch_step_b4(int group, const StepArgs& sa, bool cooperative, int nc,
+                           cudaStream_t s);
+cudaError_t launch_step_b3(int group, const StepArgs& sa, bool cooperative, int nc,
+                           cudaStream_t s);
+cudaError_t launch_step_b2(int group, const StepArgs& sa, bool cooperative, int nc,
+                           cudaStream_t s);
 
 // wq_gemm with the launch mode chosen by the caller: pdl = launch as a
 // programmatic dependent of the previous kernel on the stream (only where
@@ -121,9 +129,11 @@ wq_status_t host_sm_count(int* sms);
 wq_status_t host_check_gemm(const uint16_t* x, const uint32_t* wq, const uint16_t* scales,
                             const uint8_t* zeros, const void* y, int M, int N, int K, int group,
                             int bits, int epi);
+// Tensor maps of one projection; X boxes of nc rows.
 wq_status_t host_encode_proj(const uint16_t* x, const uint32_t* wq, const uint16_t* scales,
                              const uint8_t* zeros, int M, int N, int K, int group, int bits,
-                             CUtensorMap* tmW, CUtensorMap* tmX, int* x3d, int* meta_vec);
+                             int nc, CUtensorMap* tmW, CUtensorMap* tmX, int* x3d,
+                             int* meta_vec);
 
 // Elementwise kernels.
 cudaError_t launch_pack(const uint8_t* q, uint32_t* wq, int N, int K, int bits, int W,

@@ -24,10 +24,12 @@ namespace {
 size_t round256(size_t v) { return (v + 255) / 256 * 256; }
 
 // A run: projections [begin, end) of one bit width and group size, all with
-// M, N, K > 0 (other projections run through wq_gemm on their own).
+// M, N, K > 0 (other projections run through wq_gemm on their own); nc rows
+// of X per tile, enough for the run's largest M.
 struct Run {
     int begin, end, bits, group;
     bool fused;
+    int nc;
 };
 
 std::vector<Run> split_runs(const wq_proj_desc_t* projs, int count) {
@@ -38,8 +40,9 @@ std::vector<Run> split_runs(const wq_proj_desc_t* projs, int count) {
         if (fusable && !runs.empty() && runs.back().fused && runs.back().end == i &&
             runs.back().bits == p.bits && runs.back().group == p.group) {
             runs.back().end = i + 1;
+            runs.back().nc = std::max(runs.back().nc, wq::tc_cols(p.M));
         } else {
-            runs.push_back({i, i + 1, p.bits, p.group, fusable});
+            runs.push_back({i, i + 1, p.bits, p.group, fusable, wq::tc_cols(p.M)});
         }
     }
     return runs;
@@ -120,7 +123,7 @@ wq_status_t build_table(const wq_proj_desc_t* projs, const Run& r, std::vector<w
         const int li = i - r.begin;
         wq::ProjDev& d = out[static_cast<size_t>(li)];
         if (wq_status_t st = wq::host_encode_proj(p.x, p.wq, p.scales, p.zeros, p.M, p.N, p.K,
-                                                  p.group, p.bits, &d.tmW, &d.tmX, &d.x3d,
+                                                  p.group, p.bits, r.nc, &d.tmW, &d.tmX, &d.x3d,
                                                   &d.meta_vec))
             return st;
         // a producer before this run is complete by stream order
@@ -174,11 +177,11 @@ wq_status_t launch_run(const Run& r, Tables tab, int nphase, long long units, bo
     sa.U = units;
     sa.P = static_cast<int>(std::min<long long>(sms, units));
     if (r.bits == 4)
-        e = wq::launch_step_b4(r.group, sa, waits, s);
+        e = wq::launch_step_b4(r.group, sa, waits, r.nc, s);
     else if (r.bits == 3)
-        e = wq::launch_step_b3(r.group, sa, waits, s);
+        e = wq::launch_step_b3(r.group, sa, waits, r.nc, s);
     else
-        e = wq::launch_step_b2(r.group, sa, waits, s);
+        e = wq::launch_step_b2(r.group, sa, waits, r.nc, s);
     return e == cudaSuccess ? WQ_OK : wq::host_cuda_fail(e);
 }
 
