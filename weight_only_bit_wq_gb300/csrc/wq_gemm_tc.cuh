@@ -25,11 +25,12 @@
 //   through a matrix descriptor, fp32 D per group in tensor memory.  The zero
 //   point is applied on the tensor core: a second MMA per K step multiplies
 //   the same X by a constant A tile holding -(128 + z) in every column of the
-//   row, so each group's D is sum_k x (q - z) (where tensor memory is too
-//   small for those tiles, q - z is formed on the CUDA cores instead);
-// * epilogue warps (one per lane quarter): write the zero-point tiles, read
-//   each group's D back (tcgen05.ld), add scale * D to the row's NC fp32
-//   sums, and store Y or publish a split-K partial.
+//   row (written by the unpack warps), so each group's D is sum_k x (q - z)
+//   (where tensor memory is too small for those tiles, q - z is formed on
+//   the CUDA cores instead);
+// * epilogue warps (one per lane quarter): read each group's D back
+//   (tcgen05.ld), add scale * D to the row's NC fp32 sums, and store Y (or
+//   the gate/up activation) or publish a split-K partial.
 //
 // Tensor memory holds rings of A-tile batch slots and accumulator slots, so
 // the unpack warps run ahead of the tensor core and never wait for a result.
