@@ -75,17 +75,10 @@ constexpr int clamp_tc(int v, int lo, int hi) { return v < lo ? lo : (v > hi ? h
 // A slot only when nothing else fits; 0 if none fits.  z_only >= 0 fixes z:
 // the 32-row build keeps the 16-row build's zero-point method, whose fp32
 // rounding differs, so that rows agree bitwise between the two builds.
-// nd_first: try two accumulator slots with either zero-point method before
-// one accumulator slot.
+// z0_first: try the zero point on the CUDA cores (z = 0) first.
 constexpr int tmem_plan(int R, int a_cols, int n, int cols, int z_only = -1,
-                        bool nd_first = false) {
-    if (nd_first)
-        for (int z = 1; z >= 0; --z) {
-            if (z_only >= 0 && z != z_only) continue;
-            for (int na = 3; na >= 2; --na)
-                if (round_up_tc(na * R * (a_cols + 8 * z), 16) + 2 * R * n <= cols)
-                    return 100 * z + 10 * na + 2;
-        }
+                        bool z0_first = false) {
+    if (z0_first && z_only < 0) z_only = 0;
     for (int z = 1; z >= 0; --z) {
         if (z_only >= 0 && z != z_only) continue;
         for (int nd = 2; nd >= 1; --nd)
@@ -148,13 +141,15 @@ struct Lay {
     // Tensor memory: kNA batch slots of A tiles (plus zero-point tiles when
     // the zero point goes on the tensor core) and kND batch slots of fp32
     // accumulators, the largest plan that fits in 512 columns.
-    // 2-bit codes in groups of 32 (16 groups per stage) measured faster with
-    // two accumulator slots and the zero point on the CUDA cores (a 2-bit
-    // 5120 x 17408 GEMM at 8 rows: 22.2 -> 20.2 us) than with the zero point
-    // on the tensor core and one slot; 3-bit groups of 128 measured slower so
-    // (22.5 -> 26.8 us) and keep the default order.
+    // 2-bit codes in groups of 32 and 64 measured faster with the zero point
+    // on the CUDA cores, which leaves tensor memory for more slots (groups of
+    // 32: two accumulator slots instead of one, a 2-bit 5120 x 17408 GEMM at
+    // 8 rows 22.2 -> 20.2 us; groups of 64: three A slots instead of two,
+    // 19.15 -> 19.0 us, and 32.4 -> 31.4 us for 34816 x 5120 at 12 rows).
+    // 3-bit groups of 128 (22.5 -> 26.8 us), 3-bit groups of 32 and 4-bit
+    // groups of 64 (1.5-2.6 % slower) keep the zero point on the tensor core.
     static constexpr int kPlan16 =
-        tmem_plan(kR0, kACols, 16, int(kTmemCols), -1, BITS == 2 && G == 32);
+        tmem_plan(kR0, kACols, 16, int(kTmemCols), -1, BITS == 2 && G <= 64);
     static constexpr int kPlan =
         NC == 16 ? kPlan16 : tmem_plan(kR0, kACols, NC, int(kTmemCols), kPlan16 / 100);
     static constexpr bool kZtc = kPlan / 100 != 0;
