@@ -176,7 +176,8 @@ def _exact_gemm(x_bits, q, s_bits, z, G):
 
 
 @pytest.mark.parametrize("bits,G,K,N,M", [(4, 32, 64, 3, 1), (3, 32, 96, 5, 3), (2, 64, 128, 2, 16),
-                                          (4, 128, 256, 4, 5), (3, 64, 192, 2, 2)])
+                                          (4, 128, 256, 4, 5), (3, 64, 192, 2, 2), (4, 64, 128, 2, 32),
+                                          (2, 32, 64, 3, 24)])
 def test_gemm_brute_force_exact(bits, G, K, N, M):
     p = synth.Projection("t", M, N, K, bits, G, 100 + bits)
     w = synth.gen_weights(p)
