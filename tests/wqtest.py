@@ -57,3 +57,25 @@ def oracle_gemm(p, w, x, rows=None):
 
 def u32(t: torch.Tensor) -> np.ndarray:
     return t.cpu().numpy().view(np.uint32)
+
+
+def check_activation(got: np.ndarray, y64: np.ndarray, exact_frac: float = 0.98) -> None:
+    """The device activation against the oracle's.  The device starts from the
+    fp32 sums, which the GEMM bar lets differ from the exact ones by up to
+    ARITH_TOL x max|y|; that error passes through silu(g) * u (|silu'| < 1.1)
+    and, where g or u is near zero, can span more than one bf16 step.  So each
+    element must lie within one bf16 step plus that propagated error of the
+    oracle's value, and most elements must be bit-equal."""
+    ref = oracle.swiglu_bf16(y64)
+    assert got.shape == ref.shape
+    g, u = y64[:, 0::2], y64[:, 1::2]
+    delta = ARITH_TOL * np.abs(y64).max()
+    sig = 1.0 / (1.0 + np.exp(-g))
+    silu = g * sig
+    dsilu = sig * (1.0 + g * (1.0 - sig))
+    reff = synth.bf16_bits_to_f32(ref)
+    gotf = synth.bf16_bits_to_f32(got)
+    step = np.spacing(np.abs(reff).astype(np.float32)).astype(np.float64) * 65536.0
+    bound = step + (np.abs(dsilu * u) + np.abs(silu)) * delta
+    assert (np.abs(gotf.astype(np.float64) - reff) <= bound).all()
+    assert (got == ref).mean() > exact_frac
