@@ -1,4 +1,5 @@
-"""ctypes front end of the fp64 CPU oracle (``wq_oracle.cpp``).
+"""ctypes front end of the fp64 CPU oracle (``wq_oracle.cpp``: the GEMM and
+its epilogue; ``attn_oracle.cpp``: decode attention over a paged q8_0 KV pool).
 
 TEST INFRASTRUCTURE ONLY: imported by the tests, the smoke check and the
 benchmark's CPU-baseline leg, never by the library.  It shares no code with the
@@ -16,17 +17,18 @@ from typing import Optional
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SRC = os.path.join(_HERE, "wq_oracle.cpp")
+_SRCS = [os.path.join(_HERE, "wq_oracle.cpp"), os.path.join(_HERE, "attn_oracle.cpp")]
 _LIB = os.path.join(_HERE, "liboracle.so")
 _lib: Optional[ctypes.CDLL] = None
 
 
 def build(force: bool = False) -> str:
     """Compile liboracle.so (plain C++17, OpenMP, no FMA contraction)."""
-    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+    newest = max(os.path.getmtime(f) for f in _SRCS)
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < newest:
         tmp = _LIB + f".tmp{os.getpid()}"
         cmd = ["g++", "-std=c++17", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fopenmp",
-               "-shared", "-fPIC", "-o", tmp, _SRC]
+               "-shared", "-fPIC", "-o", tmp, *_SRCS]
         subprocess.run(cmd, check=True)
         os.replace(tmp, _LIB)
     return _LIB
@@ -52,6 +54,12 @@ def _load() -> ctypes.CDLL:
         lib.wqo_silu_f64.restype = ctypes.c_double
         lib.wqo_swiglu_bf16.argtypes = [P, i, i, P]
         lib.wqo_max_threads.argtypes = [i]
+        lib.wqo_fp16_value.argtypes = [ctypes.c_uint16]
+        lib.wqo_fp16_value.restype = ctypes.c_double
+        lib.wqo_q8_0_dequant.argtypes = [P, P, ctypes.c_long, P]
+        lib.wqo_q8_0_dequant.restype = ctypes.c_int
+        lib.wqo_paged_attention_f64.argtypes = [P, P, P, P, P, P, P, P, P] + [i] * 8 + [P]
+        lib.wqo_paged_attention_f64.restype = ctypes.c_int
         for fn in (lib.wqo_pack, lib.wqo_unpack, lib.wqo_dequant_f64, lib.wqo_dequant_bf16,
                    lib.wqo_gemm_f64, lib.wqo_max_threads):
             fn.restype = ctypes.c_int
@@ -153,3 +161,52 @@ def step_floor_seconds(weight_bytes: float, bandwidth_bytes_per_s: float) -> flo
     weights from memory once, so its time is at least bytes / bandwidth.
     """
     return weight_bytes / bandwidth_bytes_per_s
+
+
+# ------------------------------------------------------ paged decode attention
+def fp16_value(h: int) -> float:
+    """IEEE binary16 bit pattern -> value."""
+    return float(_load().wqo_fp16_value(int(h) & 0xFFFF))
+
+
+def q8_0_dequant(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """q8_0 blocks: codes int8 [..., 32 n], scales fp16 bits uint16 [..., n] ->
+    float64 [..., 32 n] with value = scale * code per block of 32."""
+    c = np.ascontiguousarray(codes, dtype=np.int8)
+    d = np.ascontiguousarray(scales, dtype=np.uint16)
+    assert c.size == 32 * d.size
+    out = np.empty(c.shape, dtype=np.float64)
+    if _load().wqo_q8_0_dequant(_ptr(c), _ptr(d), d.size, _ptr(out)):
+        raise ValueError("oracle q8_0_dequant: bad arguments")
+    return out
+
+
+def paged_attention_f64(q: np.ndarray, kc: np.ndarray, kd: np.ndarray, vc: np.ndarray,
+                        vd: np.ndarray, page_table: np.ndarray, seq_len: np.ndarray,
+                        row_seq: np.ndarray, row_pos: np.ndarray) -> np.ndarray:
+    """Decode attention over a paged q8_0 pool.
+
+    q: bf16 bits uint16 [rows][Hq][D]; kc, vc: int8 [pages][Hkv][T][D];
+    kd, vd: fp16 bits uint16 [pages][Hkv][T][D/32]; page_table: int32 [B][max_pages];
+    seq_len: int32 [B]; row_seq, row_pos: int32 [rows] (row i attends to positions
+    0 .. row_pos[i] of sequence row_seq[i]).  Returns float64 [rows][Hq][D]."""
+    q = np.ascontiguousarray(q, dtype=np.uint16)
+    kc = np.ascontiguousarray(kc, dtype=np.int8)
+    vc = np.ascontiguousarray(vc, dtype=np.int8)
+    kd = np.ascontiguousarray(kd, dtype=np.uint16)
+    vd = np.ascontiguousarray(vd, dtype=np.uint16)
+    pt = np.ascontiguousarray(page_table, dtype=np.int32)
+    sl = np.ascontiguousarray(seq_len, dtype=np.int32)
+    rs = np.ascontiguousarray(row_seq, dtype=np.int32)
+    rp = np.ascontiguousarray(row_pos, dtype=np.int32)
+    rows, Hq, D = q.shape
+    pages, Hkv, T, D2 = kc.shape
+    assert D2 == D and vc.shape == kc.shape
+    assert kd.shape == (pages, Hkv, T, D // 32) and vd.shape == kd.shape
+    B, max_pages = pt.shape
+    out = np.zeros((rows, Hq, D), dtype=np.float64)
+    if _load().wqo_paged_attention_f64(_ptr(q), _ptr(kc), _ptr(kd), _ptr(vc), _ptr(vd), _ptr(pt),
+                                       _ptr(sl), _ptr(rs), _ptr(rp), rows, B, max_pages, Hq, Hkv,
+                                       D, T, pages, _ptr(out)):
+        raise ValueError("oracle paged_attention_f64: bad arguments")
+    return out

@@ -47,7 +47,8 @@ _C2 = 0x94D049BB133111EB
 _MASK64 = (1 << 64) - 1
 
 # Stream identifiers: one independent SplitMix64 stream per tensor kind.
-STREAMS = {"q": 1, "s": 2, "z": 3, "x": 4, "outlier": 5}
+STREAMS = {"q": 1, "s": 2, "z": 3, "x": 4, "outlier": 5, "kv_code": 6, "kv_scale": 7,
+           "attn_q": 8, "page": 9}
 
 
 def _mix_int(z: int) -> int:
@@ -274,3 +275,64 @@ def gen_weights_torch(p: Projection, device, row_chunk: int = 4096):
         s32 = a32 + (b32 - a32) * u24
         s[r0:r1] = s32.to(torch.bfloat16).view(torch.int16)
     return q, s, z
+
+
+# ------------------------------------------------- paged q8_0 attention inputs
+@dataclasses.dataclass(frozen=True)
+class PagedAttention:
+    """A decode step's attention over a shared paged KV pool: sequences of
+    ``seq_lens`` tokens (the last ``rows_per_seq`` of each are this step's query
+    rows), the first ``shared_prefix`` tokens of every sequence stored once in
+    pages all sequences share."""
+    name: str
+    seq_lens: tuple
+    rows_per_seq: int
+    Hq: int
+    Hkv: int
+    D: int
+    T: int  # tokens per page
+    seed: int
+    shared_prefix: int = 0
+    spare_pages: int = 3  # pool pages no sequence uses
+    scale_range: tuple = (0.002, 0.02)
+
+
+def gen_paged_attention(p: PagedAttention) -> Dict[str, np.ndarray]:
+    """Codes U{-127..127} and fp16 scales U(scale_range) for every page of the
+    pool, bf16 N(0,1) queries, and page tables that place each sequence's
+    logical pages on distinct physical pages in a seeded shuffled order (the
+    shared prefix's pages are the same physical pages in every sequence)."""
+    B = len(p.seq_lens)
+    assert p.shared_prefix % p.T == 0 and all(n >= p.shared_prefix for n in p.seq_lens)
+    assert all(n >= p.rows_per_seq for n in p.seq_lens)
+    n_shared = p.shared_prefix // p.T
+    own = [(n - p.shared_prefix + p.T - 1) // p.T for n in p.seq_lens]
+    pages = n_shared + sum(own) + p.spare_pages
+    order = np.argsort(draws_u64(stream_key(p.seed, "page"), np.arange(pages, dtype=np.uint64)),
+                       kind="stable").astype(np.int32)
+    max_pages = max(n_shared + o for o in own)
+    table = np.zeros((B, max_pages), dtype=np.int32)
+    nxt = n_shared
+    for b in range(B):
+        table[b, :n_shared] = order[:n_shared]
+        table[b, n_shared:n_shared + own[b]] = order[nxt:nxt + own[b]]
+        nxt += own[b]
+    shape = (pages, p.Hkv, p.T, p.D)
+    n_codes = int(np.prod(shape))
+    n_scales = n_codes // 32
+    out = {}
+    for i, kv in enumerate(("k", "v")):
+        cu = draws_u64(stream_key(p.seed, "kv_code", i), np.arange(n_codes, dtype=np.uint64))
+        out[kv + "c"] = (_uniform_int(cu, 0, 254) - 127).astype(np.int8).reshape(shape)
+        su = draws_u64(stream_key(p.seed, "kv_scale", i), np.arange(n_scales, dtype=np.uint64))
+        d32 = _uniform_f32(su, *p.scale_range)
+        out[kv + "d"] = d32.astype(np.float16).view(np.uint16).reshape(shape[:3] + (p.D // 32,))
+    rows = B * p.rows_per_seq
+    qn = _normal_f32(stream_key(p.seed, "attn_q"), np.arange(rows * p.Hq * p.D, dtype=np.uint64))
+    out["q"] = f32_to_bf16_bits(qn).reshape(rows, p.Hq, p.D)
+    out["page_table"] = table
+    out["seq_len"] = np.array(p.seq_lens, dtype=np.int32)
+    out["row_seq"] = np.repeat(np.arange(B, dtype=np.int32), p.rows_per_seq)
+    out["row_pos"] = np.concatenate([np.arange(n - p.rows_per_seq, n, dtype=np.int32)
+                                     for n in p.seq_lens])
+    return out
