@@ -165,12 +165,12 @@ wq_status_t wq_gemm_swiglu(const uint16_t* x, const uint32_t* wq, const uint16_t
  * halfway through a step for lack of memory.  The caller still passes x, wq,
  * scales, zeros and y (same layout and rules as wq_gemm).
  *
- * Scratch: a fixed 4 MiB file-scope device array inside libwq, held by every
+ * Scratch: a fixed 8 MiB file-scope device array inside libwq, held by every
  * GPU that loads the library until the process exits.  The first call on a
  * device sets it up (looks up its device address and zeroes it on `stream`);
  * make that first call before any stream capture.  Every call re-zeroes the
  * per-tile counters it needs.  Problems whose scratch (wq_workspace_bytes)
- * would exceed 4 MiB — N beyond roughly 54 million rows on a 152-SM GPU — are
+ * would exceed 8 MiB — N beyond about 6.8 million rows on a 152-SM GPU — are
  * rejected with WQ_ERR_INVALID_ARG before anything is launched.  All calls
  * share the one array, so calls that overlap on the GPU (different streams,
  * or different host threads without ordering) race and give wrong results;

@@ -4,8 +4,8 @@
 #include <cudaTypedefs.h>
 
 #include <cstring>
+#include <deque>
 #include <mutex>
-#include <vector>
 
 #include "wq.h"
 #include "wq_internal.h"
@@ -28,7 +28,10 @@ struct DeviceInfo {
 };
 
 std::mutex g_mu;
-std::vector<DeviceInfo> g_dev;
+// A deque: growing it for a new device keeps earlier entries in place, so a
+// DeviceInfo* handed out for one device stays valid while another thread
+// registers a second device.
+std::deque<DeviceInfo> g_dev;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 wq_status_t device_info(DeviceInfo** out) {

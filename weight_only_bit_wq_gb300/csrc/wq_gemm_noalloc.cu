@@ -4,8 +4,8 @@
 // every GPU loading this library holds until the process exits.
 #include <cuda_runtime.h>
 
+#include <deque>
 #include <mutex>
-#include <vector>
 
 #include "wq.h"
 #include "wq_internal.h"
@@ -13,8 +13,8 @@
 namespace {
 
 // Fixed scratch size.  Enough for the split-K partials of up to 2 x (SM count)
-// CTAs (5 MB on a 152-SM GB300) plus the arrival counters of about 49,000
-// 128-row tiles.
+// CTAs (4.98 MB on a 152-SM GB300) plus the arrival counters (64 bytes per
+// tile) of about 53,000 128-row tiles, i.e. N up to about 6.8 million rows.
 constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
@@ -26,7 +26,8 @@ struct NoAllocDevice {
 };
 
 std::mutex g_noalloc_mu;
-std::vector<NoAllocDevice> g_noalloc_dev;
+// a deque keeps entries in place as devices are added (handed-out pointers stay valid)
+std::deque<NoAllocDevice> g_noalloc_dev;
 
 // One-time set-up for the current device: look up the array's device address
 // (in host code the symbol name is only a host-side stand-in) and zero it.
