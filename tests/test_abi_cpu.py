@@ -87,3 +87,56 @@ def test_elementwise_rejects_bad_arguments(wq):
                                  (1000003, 152), (272 * 20, 152), (17, 5)])
 def test_stream_k_schedule_partitions_units(wq, U, P):
     assert wq._lib().wq_internal_schedule_check(U, P) == 0
+
+
+def test_gemm_rejects_misaligned_operands(wq):
+    # x and wq feed TMA boxes: both 16-byte aligned; bf16 scales 2-byte aligned
+    lib = wq._lib()
+    bad = wq.WQ_ERR_INVALID_ARG
+    assert _gemm(lib, x=8) == bad
+    assert _gemm(lib, w=20) == bad
+    assert _gemm(lib, s=17) == bad
+    assert _gemm(lib, x=0) == bad    # null input with K > 0
+    assert _gemm(lib, z=0) == bad
+
+
+def test_swiglu_needs_gate_up_pairs(wq):
+    # rows 2j and 2j + 1 are gate and up of feature j: N must be even
+    lib = wq._lib()
+    P = ctypes.c_void_p
+    odd = lib.wq_gemm_swiglu(P(16), P(16), P(16), P(16), P(16), 4, 9, 128, 128, 4, P(0), 0, P(0))
+    assert odd == wq.WQ_ERR_INVALID_ARG
+    assert lib.wq_gemm_swiglu(P(16), P(16), P(16), P(16), P(16), 0, 8, 128, 128, 4, P(0), 0,
+                              P(0)) == wq.WQ_OK  # empty
+
+
+def _descs(wq, afters, epilogue=0, N=256):
+    arr = (wq.ProjDesc * len(afters))()
+    for i, a in enumerate(afters):
+        arr[i] = wq.ProjDesc(16, 16, 16, 16, 16, 4, N, 128, 128, 4, a, epilogue)
+    return ctypes.cast(arr, ctypes.c_void_p), len(afters)
+
+
+@pytest.mark.parametrize("afters", [[-1, 1], [0, 2, -1], [-2], [-1, 0, 5]],
+                         ids=["self", "forward", "below-minus-one", "past-end"])
+def test_step_rejects_bad_dependencies(wq, afters):
+    # a projection may only wait for an earlier one (or none: -1)
+    lib = wq._lib()
+    P = ctypes.c_void_p
+    d, n = _descs(wq, afters)
+    for flags in (0, wq.WQ_STEP_FUSED):
+        assert lib.wq_step_run_ex(d, n, flags, P(16), 1 << 20, P(0)) == wq.WQ_ERR_INVALID_ARG
+    g = P(0)
+    assert lib.wq_step_graph_create_ex(d, n, 0, P(16), 1 << 20, P(0),
+                                       ctypes.byref(g)) == wq.WQ_ERR_INVALID_ARG
+
+
+def test_step_rejects_bad_flags_and_epilogues(wq):
+    lib = wq._lib()
+    P = ctypes.c_void_p
+    d, n = _descs(wq, [-1, 0])
+    assert lib.wq_step_run_ex(d, n, 0x10, P(16), 1 << 20, P(0)) == wq.WQ_ERR_INVALID_ARG
+    d, n = _descs(wq, [-1], epilogue=7)
+    assert lib.wq_step_run_ex(d, n, 0, P(16), 1 << 20, P(0)) == wq.WQ_ERR_INVALID_ARG
+    d, n = _descs(wq, [-1], epilogue=wq.WQ_EPI_SWIGLU, N=255)  # odd gate/up width
+    assert lib.wq_step_run_ex(d, n, 0, P(16), 1 << 20, P(0)) == wq.WQ_ERR_INVALID_ARG
