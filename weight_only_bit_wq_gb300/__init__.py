@@ -222,7 +222,8 @@ def new_step_workspace(descs: ctypes.Array, flags: int = 0, device=None) -> torc
 
 def wq_step_run(descs: ctypes.Array, workspace: torch.Tensor, stream=None, flags: int = 0) -> None:
     _check(_lib().wq_step_run_ex(ctypes.cast(descs, ctypes.c_void_p), len(descs), flags,
-                                 _ptr(workspace), workspace.numel(), _stream(stream)),
+                                 _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                 _stream(stream)),
            "wq_step_run_ex")
 
 
@@ -234,7 +235,8 @@ class StepGraph:
         self._ws = workspace
         h = ctypes.c_void_p(0)
         _check(_lib().wq_step_graph_create_ex(ctypes.cast(descs, ctypes.c_void_p), len(descs),
-                                              flags, _ptr(workspace), workspace.numel(),
+                                              flags, _ptr(workspace),
+                                              workspace.numel() * workspace.element_size(),
                                               _stream(stream), ctypes.byref(h)),
                "wq_step_graph_create_ex")
         self._h = h
