@@ -448,8 +448,9 @@ def cpu_sample(M, row_budget):
     return sample
 
 
-def time_oracle(sample, seconds, passes=None):
-    """Time full oracle passes (pack + fp64 GEMM) over the sample on all host cores."""
+def time_oracle(sample, seconds, passes=None, threads=0):
+    """Time full oracle passes (pack + fp64 GEMM) over the sample on all host cores
+    (or on `threads` of them)."""
     import oracle
 
     packed = sum(ps.N * oracle.words_per_row(ps.K, ps.bits) * 4 for ps, *_ in sample)
@@ -458,26 +459,58 @@ def time_oracle(sample, seconds, passes=None):
     while True:
         t1 = time.perf_counter()
         for ps, q, s, z, x in sample:
-            oracle.gemm_f64(x, oracle.pack(q, ps.bits), s, z, ps.K, ps.group, ps.bits)
+            oracle.gemm_f64(x, oracle.pack(q, ps.bits), s, z, ps.K, ps.group, ps.bits, threads)
         times.append(time.perf_counter() - t1)
         done += 1
         if passes is not None and done >= passes:
             break
         if passes is None and time.perf_counter() - t0 >= seconds:
             break
-    return packed, times, oracle.max_threads()
+    return packed, times, oracle.max_threads(threads)
+
+
+def cpu_model():
+    """The host CPU's model from /proc/cpuinfo (x86 model name, or Arm implementer and part)."""
+    import re
+
+    try:
+        with open("/proc/cpuinfo") as f:
+            text = f.read()
+    except OSError:
+        return None
+    m = re.search(r"^model name\s*:\s*(.+)$", text, re.M)
+    if m:
+        return m.group(1).strip()
+    imp = re.search(r"^CPU implementer\s*:\s*(\S+)$", text, re.M)
+    part = re.search(r"^CPU part\s*:\s*(\S+)$", text, re.M)
+    if imp and part:
+        return f"Arm implementer {imp.group(1)}, part {part.group(1)}"
+    return None
 
 
 def cpu_baseline(M, seconds):
+    import oracle
+
     sample = cpu_sample(M, 2048)
-    time_oracle(sample, 0, passes=1)  # warm-up
-    packed, times, cores = time_oracle(sample, seconds)
+    cores = oracle.max_threads()
+    time_oracle(sample, 0, passes=1, threads=cores)  # warm-up
+    packed, times, cores = time_oracle(sample, seconds, threads=cores)
     gbs = packed * len(times) / sum(times) / 1e9
     desc = (f"layer-0 gate/up rows 0..{sample[0][0].N - 1} and down rows 0..{sample[1][0].N - 1} "
             f"at M={M} ({packed / 1e6:.1f} MB packed per pass, {len(times)} passes, "
             f"pack + fp64 GEMM)")
-    return {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-            "sample": desc}
+    out = {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+           "sample": desc, "cpu_model": cpu_model()}
+    # the same sample on one core, for the scaling of the oracle itself (context only)
+    try:
+        _, t1, _ = time_oracle(sample, seconds / 4, threads=1)
+        out["single_thread_value"] = round(packed * len(t1) / sum(t1) / 1e9, 4)
+    except Exception as e:  # context only: never fail the benchmark over it
+        out["single_thread_value"] = None
+        out["single_thread_error"] = str(e)[:200]
+    finally:
+        time_oracle(sample, 0, passes=1, threads=cores)  # leave the oracle on all cores
+    return out
 
 
 # ------------------------------------------------------------------- main
