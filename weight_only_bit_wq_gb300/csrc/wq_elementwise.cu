@@ -57,8 +57,10 @@ __global__ void unpack_kernel(const uint32_t* __restrict__ wq, uint8_t* __restri
     }
 }
 
-// w = RNE_bf16((q - z) * s).  (q - z) has at most 5 significant bits and s is a
-// bf16 (8 bits), so the fp32 product is exact and the cast is the only rounding.
+// w = RNE_bf16((q - z) * s).  q - z is an integer with |q - z| <= 255 (8
+// significant bits for any uint8 zero point, at most 5 for the documented
+// range) and s is a bf16 (8 bits), so the fp32 product is exact and the cast
+// is the only rounding.
 __global__ void dequant_kernel(const uint32_t* __restrict__ wq, const uint16_t* __restrict__ scales,
                                const uint8_t* __restrict__ zeros, uint16_t* __restrict__ w, int N,
                                int K, int group, int bits, int W) {
