@@ -29,7 +29,12 @@
  *                                words that round a row up to a multiple of 4
  *                                words (16 bytes) are zero
  *   scales  bf16   [N][K/G]      per-group scale s (bf16 bit patterns, uint16)
- *   zeros   uint8  [N][K/G]      per-group zero point z
+ *   zeros   uint8  [N][K/G]      per-group zero point z: in [0, 2^bits - 1] as
+ *                                the codes (any z <= 127 works); wq_gemm and the
+ *                                step driver form 128 + z as a bf16 bit pattern,
+ *                                so z >= 128 gives wrong results there (device
+ *                                data: not checked); wq_dequant is exact for
+ *                                any uint8
  *   x       bf16   [M][K]        activations (bf16 bit patterns)
  *   y       fp32   [M][N]        output
  *   w       bf16   [N][K]        dequantised weights (wq_dequant output)
