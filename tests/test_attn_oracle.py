@@ -152,6 +152,23 @@ def test_page_placement_does_not_matter():
     assert (got2 == got).all()
 
 
+def test_sequence_and_row_order_do_not_matter():
+    # relabelling the sequences (page-table rows and lengths) and listing the
+    # query rows in another order moves each row's result with it
+    d = synth.gen_paged_attention(CASE)
+    got = _run(d)
+    B = len(CASE.seq_lens)
+    sp = np.array([2, 0, 1])[:B]             # new label of old sequence b
+    inv = np.argsort(sp)                      # old sequence of new label
+    rp = np.random.default_rng(4).permutation(len(d["row_seq"]))  # new row i = old row rp[i]
+    got2 = _run(d, page_table=np.ascontiguousarray(d["page_table"][inv]),
+                seq_len=np.ascontiguousarray(d["seq_len"][inv]),
+                row_seq=np.ascontiguousarray(sp[d["row_seq"][rp]].astype(np.int32)),
+                row_pos=np.ascontiguousarray(d["row_pos"][rp]),
+                q=np.ascontiguousarray(d["q"][rp]))
+    assert (got2 == got[rp]).all()
+
+
 def test_duplicated_kv_heads_give_the_same_attention():
     d = synth.gen_paged_attention(CASE)
     got = _run(d)
