@@ -179,11 +179,23 @@ wq_status_t wq_gemm_swiglu(const uint16_t* x, const uint32_t* wq, const uint16_t
  * rejected with WQ_ERR_INVALID_ARG before anything is launched.  All calls
  * share the one array, so calls that overlap on the GPU (different streams,
  * or different host threads without ordering) race and give wrong results;
- * order them on one stream.  Nothing is allocated or freed.
+ * order them on one stream.  Nothing is allocated or freed.  The kernel's
+ * error word (a bounded wait that ran out) sits in the same array: read it
+ * with wq_check_noalloc.
  */
 wq_status_t wq_gemm_noalloc(const uint16_t* x, const uint32_t* wq, const uint16_t* scales,
                             const uint8_t* zeros, float* y, int M, int N, int K, int group,
                             int bits, void* stream);
+
+/*
+ * wq_check_noalloc — the error word of wq_gemm_noalloc's fixed array on the
+ * current device, read after synchronising `stream`: WQ_OK, or WQ_ERR_TIMEOUT
+ * if a wq_gemm_noalloc kernel abandoned a bounded wait since the last check
+ * (its y is then wrong).  Clears the word and, after WQ_ERR_TIMEOUT, zeroes
+ * the whole array (no allocation).  WQ_OK before the first call on a device.
+ * The paper has no counterpart (see wq_gemm_noalloc).
+ */
+wq_status_t wq_check_noalloc(void* stream);
 
 /*
  * Read back the kernel error word of a workspace (NULL = the library buffer

@@ -3,10 +3,12 @@
 pool, or a step that must not allocate part-way through).  It keeps its scratch
 in a fixed array inside the library instead of a workspace argument.
 
-This file is collected last on purpose.  Its checks: through the C ABI, two
-calls in a row agree with wq_gemm within the GEMM tolerance (the second call
-sees whatever the first left in the shared array), and a problem too large for
-the fixed array is refused up front.
+This file is collected last on purpose.  Its checks, through the C ABI: two
+calls in a row give Y bit for bit equal to wq_gemm's (the same kernel with the
+same split; the second call sees whatever the first left in the shared array)
+and within the GEMM tolerance of the fp64 oracle; the array's error word reads
+back clean (wq_check_noalloc); and a problem too large for the fixed array is
+refused up front.
 """
 import ctypes
 
@@ -15,7 +17,7 @@ import pytest
 import torch
 
 import synth
-from wqtest import ARITH_TOL, REL_TOL, dev, rel_err, to_dev_host_inputs
+from wqtest import ARITH_TOL, REL_TOL, dev, oracle_gemm, rel_err, to_dev_host_inputs
 
 pytestmark = pytest.mark.gpu
 
@@ -29,17 +31,23 @@ def lib():
     P, I = ctypes.c_void_p, ctypes.c_int
     L.wq_gemm_noalloc.argtypes = [P, P, P, P, P, I, I, I, I, I, P]
     L.wq_gemm_noalloc.restype = I
+    L.wq_check_noalloc.argtypes = [P]
+    L.wq_check_noalloc.restype = I
     return L
 
 
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
 def _call(lib, d, y, p):
-    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     return lib.wq_gemm_noalloc(ctypes.c_void_p(d["x"].data_ptr()), ctypes.c_void_p(d["wq"].data_ptr()),
                                ctypes.c_void_p(d["s"].data_ptr()), ctypes.c_void_p(d["z"].data_ptr()),
-                               ctypes.c_void_p(y.data_ptr()), p.M, p.N, p.K, p.group, p.bits, stream)
+                               ctypes.c_void_p(y.data_ptr()), p.M, p.N, p.K, p.group, p.bits,
+                               _stream())
 
 
-def test_noalloc_matches_wq_gemm_twice(lib):
+def test_noalloc_matches_wq_gemm_and_oracle_twice(lib):
     import weight_only_bit_wq_gb300 as wq
     # first a shape whose tiles are split across CTAs, then a different one
     cases = [synth.Projection("a", 12, 3000, 5120, 4, 128, 901, outlier_frac=0.01),
@@ -47,18 +55,23 @@ def test_noalloc_matches_wq_gemm_twice(lib):
     for p in cases:
         w, x, d = to_dev_host_inputs(p)
         ref = wq.wq_gemm(d["x"], d["wq"], d["s"], d["z"], p.N, p.group, p.bits).cpu().numpy()
+        y_ref = oracle_gemm(p, w, x)
         for _ in range(2):
             y = torch.full((p.M, p.N), float("nan"), dtype=torch.float32, device=dev())
             assert _call(lib, d, y, p) == wq.WQ_OK
             got = y.cpu().numpy()
-            err = rel_err(got, ref.astype(np.float64))
+            # same kernel, same split, same reduction order: bit for bit
+            assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+            err = rel_err(got, y_ref)
             assert err <= REL_TOL and err <= ARITH_TOL, err
+        assert lib.wq_check_noalloc(_stream()) == wq.WQ_OK
 
 
 def test_noalloc_refuses_oversized_problem(lib):
     import weight_only_bit_wq_gb300 as wq
-    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     P = ctypes.c_void_p
-    # 2^30 rows need 32 MiB of tile counters: far beyond the fixed array
-    st = lib.wq_gemm_noalloc(P(16), P(16), P(16), P(16), P(16), 1, 1 << 30, 128, 128, 4, stream)
+    # 2^30 rows = 2^23 tiles x 64 bytes of arrival counters = 512 MiB: far beyond
+    # the fixed 8 MiB array; refused before anything is launched
+    st = lib.wq_gemm_noalloc(P(16), P(16), P(16), P(16), P(16), 1, 1 << 30, 128, 128, 4, _stream())
     assert st == wq.WQ_ERR_INVALID_ARG
+    assert lib.wq_check_noalloc(_stream()) == wq.WQ_OK

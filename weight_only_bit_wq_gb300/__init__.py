@@ -24,7 +24,8 @@ WQ_OK, WQ_ERR_INVALID_ARG, WQ_ERR_UNSUPPORTED, WQ_ERR_CUDA, WQ_ERR_TIMEOUT = ran
 
 EXPORTED = ("wq_abi_version", "wq_status_string", "wq_last_cuda_error", "wq_packed_words_per_row",
             "wq_pack", "wq_unpack", "wq_dequant", "wq_workspace_bytes", "wq_workspace_init",
-            "wq_gemm", "wq_gemm_swiglu", "wq_check_workspace", "wq_step_workspace_bytes", "wq_step_run",
+            "wq_gemm", "wq_gemm_swiglu", "wq_check_workspace", "wq_gemm_noalloc", "wq_check_noalloc",
+            "wq_step_workspace_bytes", "wq_step_run",
             "wq_step_run_ex", "wq_step_graph_create", "wq_step_graph_create_ex",
             "wq_step_graph_launch", "wq_step_graph_destroy")
 
@@ -74,6 +75,8 @@ def _lib() -> ctypes.CDLL:
             "wq_gemm": ([P, P, P, P, P, I, I, I, I, I, P, S, P], I),
             "wq_gemm_swiglu": ([P, P, P, P, P, I, I, I, I, I, P, S, P], I),
             "wq_check_workspace": ([P, P], I),
+            "wq_gemm_noalloc": ([P, P, P, P, P, I, I, I, I, I, P], I),
+            "wq_check_noalloc": ([P], I),
             "wq_step_workspace_bytes": ([P, I, ctypes.c_uint], S),
             "wq_step_run": ([P, I, P, S, P], I),
             "wq_step_run_ex": ([P, I, ctypes.c_uint, P, S, P], I),
@@ -193,6 +196,22 @@ def wq_gemm_swiglu(x, wq, scales, zeros, N: int, group: int, bits: int, out=None
 
 def wq_check_workspace(workspace=None, stream=None) -> None:
     _check(_lib().wq_check_workspace(_ptr(workspace), _stream(stream)), "wq_check_workspace")
+
+
+def wq_gemm_noalloc(x, wq, scales, zeros, N: int, group: int, bits: int, out=None,
+                    stream=None) -> torch.Tensor:
+    """wq_gemm with its scratch in the library's fixed device array (no device allocation
+    inside libwq; `out`, if given, is the caller's fp32 [M][N] buffer)."""
+    M, K = x.shape
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    _check(_lib().wq_gemm_noalloc(_ptr(x), _ptr(wq), _ptr(scales), _ptr(zeros), _ptr(out), M, N,
+                                  K, group, bits, _stream(stream)), "wq_gemm_noalloc")
+    return out
+
+
+def wq_check_noalloc(stream=None) -> None:
+    _check(_lib().wq_check_noalloc(_stream(stream)), "wq_check_noalloc")
 
 
 def make_descs(projs: Sequence[dict]) -> ctypes.Array:
