@@ -203,3 +203,17 @@ def test_extreme_shapes_sampled_rows(fmt, M, N, K):
     ref = oracle.gemm_f64(x, oracle.pack(w["q"], bits), w["s"], w["z"], K, G, bits)
     got = y.cpu().numpy()[:, rows]
     assert rel_err(got, ref) <= REL_TOL
+
+
+@pytest.mark.parametrize("fmt", [(4, 128), (2, 64), (3, 32)], ids=_fid)
+def test_largest_supported_zero_point(fmt):
+    # z up to 127 is exact in every kernel build (128 + z is an 8-bit bf16
+    # mantissa pattern); here every zero point is 120..127
+    wq = _wq()
+    bits, G = fmt
+    p = proj("C3", M=6, N=260, K=1024, bits=bits, group=G, outlier_frac=0.0, z_range=(120, 127))
+    w, x, d = to_dev_host_inputs(p)
+    y = wq.wq_gemm(d["x"], d["wq"], d["s"], d["z"], p.N, G, bits)
+    torch.cuda.synchronize()
+    ref = oracle.gemm_f64(x, oracle.pack(w["q"], bits), w["s"], w["z"], p.K, G, bits)
+    assert rel_err(y.cpu().numpy(), ref) <= REL_TOL
