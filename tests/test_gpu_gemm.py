@@ -179,3 +179,41 @@ def test_extreme_codes_and_zero_points():
                        torch.from_numpy(s.view(np.int16)).to(d), torch.from_numpy(z).to(d), N, G, bits)
         y_ref = oracle.gemm_f64(x, oracle.pack(q, bits), s, z, K, G, bits)
         assert rel_err(y.cpu().numpy(), y_ref) <= ARITH_TOL
+
+
+@pytest.mark.parametrize("fmt,M,N,K", [((4, 128), 16, 128, 65536), ((2, 32), 7, 160, 32768),
+                                       ((3, 128), 12, 300160, 256)],
+                         ids=["long-K-one-tile", "long-K-2bit", "tall-N"])
+def test_extreme_shapes_sampled_rows(fmt, M, N, K):
+    # one 128-row tile split over the most CTAs a tile may have (long K), and
+    # thousands of tiles with a short K (tall N): sampled weight rows against
+    # the oracle
+    wq = _wq()
+    bits, G = fmt
+    p = proj("C3", M=M, N=N, K=K, bits=bits, group=G, outlier_frac=0.0)
+    q, s, z = synth.gen_weights_torch(p, dev())
+    wq_d = wq.wq_pack(q, bits)
+    del q
+    x = synth.gen_x(p)
+    y = wq.wq_gemm(torch.from_numpy(x.view(np.int16)).to(dev()), wq_d, s, z, N, G, bits)
+    torch.cuda.synchronize()
+    wq.wq_check_workspace()
+    rows = np.unique(np.linspace(0, N - 1, 24).astype(np.int64))
+    w = synth.gen_weights(p, rows=rows)
+    ref = oracle.gemm_f64(x, oracle.pack(w["q"], bits), w["s"], w["z"], K, G, bits)
+    got = y.cpu().numpy()[:, rows]
+    assert rel_err(got, ref) <= REL_TOL
+
+
+@pytest.mark.parametrize("fmt", [(4, 128), (2, 64), (3, 32)], ids=_fid)
+def test_largest_supported_zero_point(fmt):
+    # z up to 127 is exact in every kernel build (128 + z is an 8-bit bf16
+    # mantissa pattern); here every zero point is 120..127
+    wq = _wq()
+    bits, G = fmt
+    p = proj("C3", M=6, N=260, K=1024, bits=bits, group=G, outlier_frac=0.0, z_range=(120, 127))
+    w, x, d = to_dev_host_inputs(p)
+    y = wq.wq_gemm(d["x"], d["wq"], d["s"], d["z"], p.N, G, bits)
+    torch.cuda.synchronize()
+    ref = oracle.gemm_f64(x, oracle.pack(w["q"], bits), w["s"], w["z"], p.K, G, bits)
+    assert rel_err(y.cpu().numpy(), ref) <= REL_TOL
