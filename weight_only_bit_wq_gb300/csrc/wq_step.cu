@@ -232,8 +232,12 @@ wq_status_t upload_tables(const wq_proj_desc_t* projs, int count, void* base) {
 // Fused step.  With `tables` (device, uploaded by upload_tables) the launches
 // read those; without, each run's tables are staged into the workspace's
 // table area (slots per projection, so no run overwrites another's) first.
+// stall_first_phase: test hook only (wq_internal_step_stall_probe): phase 0
+// of every run gets a completion threshold no launch reaches, so the
+// projections waiting for it run out their bounded waits.
 wq_status_t run_fused(const wq_proj_desc_t* projs, int count, void* workspace,
-                      size_t workspace_bytes, cudaStream_t s, void* tables) {
+                      size_t workspace_bytes, cudaStream_t s, void* tables,
+                      bool stall_first_phase = false) {
     int sms = 0;
     if (wq_status_t st = wq::host_sm_count(&sms)) return st;
     const std::vector<Run> runs = split_runs(projs, count);
@@ -253,6 +257,7 @@ wq_status_t run_fused(const wq_proj_desc_t* projs, int count, void* workspace,
         long long units = 0;
         bool waits = false;
         if (wq_status_t st = build_table(projs, r, host, phases, &units, &waits)) return st;
+        if (stall_first_phase && phases.size() > 1) phases[0].need = 0x7fffffff;
         if (!tables) {
             // pageable sources: each copy is staged before the call returns
             cudaError_t e = cudaMemcpyAsync(tab.proj + r.begin, host.data(),
@@ -375,6 +380,19 @@ void wq_step_graph_destroy(wq_step_graph_t g) {
     if (g->graph) cudaGraphDestroy(g->graph);
     if (g->tables) cudaFree(g->tables);
     delete g;
+}
+
+// Test hook for the bounded-wait path (not part of include/wq.h): runs the
+// fused step like wq_step_run_ex(WQ_STEP_FUSED) but with phase 0 of every run
+// never reported complete, so every projection that waits for it gives up
+// after the kernels' wait limit and the workspace's error word reads
+// WQ_ERR_TIMEOUT through wq_check_workspace.  Nothing faults or traps: the
+// waits end, the CTAs free their tensor memory and exit.
+wq_status_t wq_internal_step_stall_probe(const wq_proj_desc_t* projs, int count, void* workspace,
+                                         size_t workspace_bytes, void* stream) {
+    if (wq_status_t st = check_all(projs, count)) return st;
+    return run_fused(projs, count, workspace, workspace_bytes,
+                     reinterpret_cast<cudaStream_t>(stream), nullptr, true);
 }
 
 }  // extern "C"
