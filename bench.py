@@ -385,6 +385,34 @@ def run_dominant(stack, M, stream, steps, warmup, dist):
     return ms / len(sel), proj_bytes(M, d["N"], d["K"], d["group"], d["bits"]), len(sel)
 
 
+CONFIG_MIN_CALLS = 200  # calls timed per config
+
+
+def graph_call_times(launch, stream, launches, warmup, calls_per_launch):
+    """µs per call of each of `launches` timed graph launches (CUDA events between
+    consecutive launches on the launching stream)."""
+    import torch
+
+    for _ in range(warmup):
+        launch()
+    stream.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(launches + 1)]
+    ev[0].record(stream)
+    for i in range(launches):
+        launch()
+        ev[i + 1].record(stream)
+    ev[-1].synchronize()
+    return [ev[i].elapsed_time(ev[i + 1]) * 1e3 / calls_per_launch for i in range(launches)]
+
+
+def percentiles(samples):
+    """Median, 10th and 90th percentile (linear interpolation)."""
+    import numpy as np
+
+    a = np.asarray(samples, dtype=np.float64)
+    return float(np.median(a)), float(np.percentile(a, 10)), float(np.percentile(a, 90))
+
+
 def run_configs(device, stream, peak, l2_bytes):
     """Single-call figures for the seeded configs, rotating weight copies past L2."""
     import numpy as np
@@ -415,14 +443,16 @@ def run_configs(device, stream, peak, l2_bytes):
                                     K=p.K, group=p.group, bits=p.bits) for c in copies])
         stream.wait_stream(torch.cuda.current_stream())
         g = wq.StepGraph(descs, ws, stream=stream)
-        ms = time_launches(lambda: g.launch(stream=stream), stream, 5, 2, None) / reps
+        launches = max(5, -(-CONFIG_MIN_CALLS // reps))
+        per_call = graph_call_times(lambda: g.launch(stream=stream), stream, launches, 2, reps)
         g.close()
-        us = ms * 1e3
+        us, p10, p90 = percentiles(per_call)
         out[name] = {"M": p.M, "N": p.N, "K": p.K, "bits": p.bits, "group": p.group,
-                     "us_per_call": round(us, 3),
+                     "us_per_call": round(us, 3), "us_p10": round(p10, 3), "us_p90": round(p90, 3),
                      "weight_gbs": round(b["packed"] / (us * 1e-6) / 1e9, 1),
                      "roofline_frac": round(b["total"] / (us * 1e-6) / 1e9 / peak, 4),
-                     "bytes_per_call": b["total"], "rotated_copies": reps}
+                     "bytes_per_call": b["total"], "rotated_copies": reps,
+                     "timed_calls": launches * reps}
         del copies, descs
         torch.cuda.empty_cache()
     return out
