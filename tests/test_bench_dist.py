@@ -61,3 +61,14 @@ def test_config_percentiles_and_call_counts():
     for reps in (1, 6, 12, 21, 977):
         launches = max(5, -(-bench.CONFIG_MIN_CALLS // reps))
         assert launches * reps >= bench.CONFIG_MIN_CALLS and launches >= 5
+
+
+def test_headline_mode_is_the_faster_chain_mode():
+    import bench
+
+    assert bench.choose_head({"fused": 5.17, "sequential": 4.96}) == "sequential"
+    assert bench.choose_head({"fused": 4.0, "sequential": 4.96}) == "fused"
+    assert bench.choose_head({"fused": 5.0, "sequential": 5.0}) == "fused"
+    cfg = bench._config(16, 64, 1, "sequential", 384)
+    assert cfg["launches_per_step"] == 384 and "sequential" in cfg["headline"]
+    assert bench._config(16, 64, 1)["launches_per_step"] == 1
