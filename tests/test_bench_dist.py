@@ -50,3 +50,25 @@ def test_single_process_is_identity():
     assert bench.dist_init(1, "gloo") is None
     gbs, ms, total = bench.whole_job_gbs(None, 2e9, 4.0)
     assert (ms, total) == (4.0, 2e9) and gbs == pytest.approx(500.0)
+
+
+def test_config_percentiles_and_call_counts():
+    import bench
+
+    med, p10, p90 = bench.percentiles([5.0, 1.0, 4.0, 2.0, 3.0])
+    assert (med, p10, p90) == (3.0, 1.4, 4.6)
+    # every config times at least CONFIG_MIN_CALLS calls, in whole graph launches
+    for reps in (1, 6, 12, 21, 977):
+        launches = max(5, -(-bench.CONFIG_MIN_CALLS // reps))
+        assert launches * reps >= bench.CONFIG_MIN_CALLS and launches >= 5
+
+
+def test_headline_mode_is_the_faster_chain_mode():
+    import bench
+
+    assert bench.choose_head({"fused": 5.17, "sequential": 4.96}) == "sequential"
+    assert bench.choose_head({"fused": 4.0, "sequential": 4.96}) == "fused"
+    assert bench.choose_head({"fused": 5.0, "sequential": 5.0}) == "fused"
+    cfg = bench._config(16, 64, 1, "sequential", 384)
+    assert cfg["launches_per_step"] == 384 and "sequential" in cfg["headline"]
+    assert bench._config(16, 64, 1)["launches_per_step"] == 1
