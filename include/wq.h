@@ -279,7 +279,7 @@ void wq_step_graph_destroy(wq_step_graph_t graph);
  *
  * Layout (device pointers): q bf16 [rows][Hq][D]; k_codes, v_codes int8
  * [pages][Hkv][T][D] (16-byte aligned); k_scales, v_scales binary16
- * [pages][Hkv][T][D/32]; page_table int32 [B][max_pages] (sequence b's token t
+ * [pages][Hkv][T][D/32] (8-byte aligned); page_table int32 [B][max_pages] (sequence b's token t
  * in physical page page_table[b][t / T], slot t % T; pages may be shared);
  * seq_len int32 [B]; row_seq, row_pos int32 [rows]; out fp32 [rows][Hq][D].
  * D = 128; Hq a multiple of Hkv with Hq / Hkv <= 16; max_seq_len (host) bounds

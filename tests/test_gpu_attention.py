@@ -3,6 +3,7 @@ heads, pages shared by a common prefix and placed in shuffled order, draft
 rows seeing only earlier positions, long sequences split across CTAs, bitwise
 determinism, and a table entry outside the pool reported in the error word.
 All calls go through the C ABI."""
+import ctypes
 import dataclasses
 
 import numpy as np
@@ -35,13 +36,35 @@ def _to_dev(d):
     return t
 
 
-def _run(d, max_seq_len=None, workspace=None):
+def _cuda_cores(wq):
+    # the CUDA-core kernel (fp32 FMA), exported for cross-checks only
+    fn = wq._lib().wq_internal_paged_attention_cuda_cores
+    fn.argtypes = wq._lib().wq_paged_attention.argtypes
+    fn.restype = ctypes.c_int
+    return fn
+
+
+def _run(d, max_seq_len=None, workspace=None, cuda_cores=False):
     import weight_only_bit_wq_gb300 as wq
     t = _to_dev(d)
     msl = int(d["seq_len"].max()) if max_seq_len is None else max_seq_len
-    out = wq.wq_paged_attention(t["q"], t["kc"], t["kd"], t["vc"], t["vd"], t["page_table"],
-                                t["seq_len"], t["row_seq"], t["row_pos"], msl,
-                                workspace=workspace)
+    if not cuda_cores:
+        out = wq.wq_paged_attention(t["q"], t["kc"], t["kd"], t["vc"], t["vd"], t["page_table"],
+                                    t["seq_len"], t["row_seq"], t["row_pos"], msl,
+                                    workspace=workspace)
+    else:
+        rows, Hq, D = t["q"].shape
+        pages, Hkv, T, _ = t["kc"].shape
+        B, max_pages = t["page_table"].shape
+        out = torch.empty((rows, Hq, D), dtype=torch.float32, device=dev())
+        n = int(wq._lib().wq_paged_attention_workspace_bytes(rows, Hq, msl))
+        ws = torch.zeros(max(n, 256), dtype=torch.uint8, device=dev())
+        p = lambda x: ctypes.c_void_p(x.data_ptr())
+        st = _cuda_cores(wq)(p(t["q"]), p(t["kc"]), p(t["kd"]), p(t["vc"]), p(t["vd"]),
+                             p(t["page_table"]), max_pages, p(t["seq_len"]), B, p(t["row_seq"]),
+                             p(t["row_pos"]), rows, msl, Hq, Hkv, D, T, pages, p(out), p(ws),
+                             ws.numel(), ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+        assert st == 0
     torch.cuda.synchronize()
     return out.cpu().numpy()
 
@@ -59,12 +82,35 @@ CASES = [
 ]
 
 
+@pytest.mark.parametrize("cuda_cores", [False, True], ids=["tensor-cores", "cuda-cores"])
 @pytest.mark.parametrize("p", CASES, ids=lambda p: p.name)
-def test_attention_matches_oracle(p):
+def test_attention_matches_oracle(p, cuda_cores):
     d = synth.gen_paged_attention(p)
-    got = _run(d)
+    got = _run(d, cuda_cores=cuda_cores)
     ref = _oracle(d)
     assert np.abs(got - ref).max() <= TOL * np.abs(ref).max()
+
+
+def _scaled_queries(d, factor):
+    # bf16 queries times a power of two (exact)
+    q = (d["q"].astype(np.uint32) << 16).view(np.float32) * np.float32(factor)
+    return (q.view(np.uint32) >> 16).astype(np.uint16)
+
+
+@pytest.mark.parametrize("scale_range,q_factor", [((1e-5, 8.0), 1.0), ((0.002, 0.02), 32.0),
+                                                  ((1e-4, 1e-3), 2.0 ** -7)],
+                         ids=["wide-scales", "peaked", "small"])
+def test_attention_extreme_ranges(scale_range, q_factor):
+    # value scales over six decades, sharply peaked softmax (large queries),
+    # and small queries with small scales: the binary16 operands of the
+    # tensor-core kernel keep their bits through the power-of-two scalings
+    p = dataclasses.replace(CASES[0], scale_range=scale_range)
+    d = dict(synth.gen_paged_attention(p))
+    d["q"] = _scaled_queries(d, q_factor)
+    ref = _oracle(d)
+    for cc in (False, True):
+        got = _run(d, cuda_cores=cc)
+        assert np.abs(got - ref).max() <= TOL * np.abs(ref).max(), cc
 
 
 def test_attention_is_deterministic_and_placement_free():

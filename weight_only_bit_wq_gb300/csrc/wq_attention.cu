@@ -4,7 +4,9 @@
 // shared pool of 132K tokens in q8_0, managed in pages, a common system
 // prompt stored once).
 //
-// First CUDA path: flash-decoding on the CUDA cores.  A CTA takes one
+// Two split kernels with one structure; the entry point runs the tensor-core
+// one (described above attn_split_tc_kernel), and the CUDA-core one is kept as
+// an independent cross-check.  CUDA-core kernel: flash-decoding.  A CTA takes one
 // (sequence, key/value head, slice of positions); its four warps walk the
 // slice 32 positions at a time, one position per lane for the scores (the
 // query vectors of the sequence's rows for the head's query heads sit in
@@ -216,6 +218,353 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnArgs a) 
     }
 }
 
+// ------------------------------------------------------------ tensor-core path
+// The same CTA, slice and pass structure on the tensor cores (mma.sync
+// m16n8k16, binary16 operands, fp32 accumulators).  Each warp takes 16
+// positions at a time:
+//   scores  S[16 query vectors][8 positions] per n-tile, k running over head
+//           dims.  The query vectors are multiplied by a power of two 2^eq
+//           (per pass) that puts the largest in [2^14, 2^15), so every bf16
+//           query value is exact in binary16 unless it is 2^-32 times smaller
+//           than the largest; the codes are exact in binary16.  Each 32-dim
+//           block is summed on its own and multiplied by its position's scale
+//           in fp32 (the scale varies along positions, the n side).
+//   values  O[16 query vectors][8 dims] per n-tile, k running over the 16
+//           positions.  The value scale varies along k, so it goes into A: for
+//           the n-tile's 32-dim block, A = p * scale * 2^ev, with 2^ev keeping
+//           the chunk's largest scale below 2^15, split into its binary16
+//           rounding and the binary16 rounding of the remainder (two MMAs,
+//           about 22 significant bits); O carries 2^ev until the end.
+// The head dims are assigned to k (and, for the values, to n) in a permuted
+// order so that each lane's codes come from one 8-byte (keys) or 4-byte
+// (values) load: for k-step 2 * blk + hh, lane quad position c holds k =
+// 2c, 2c + 1 as dims 32 blk + 8c + 4hh + {0, 1} and k = 2c + 8, 2c + 9 as
+// dims 32 blk + 8c + 4hh + {2, 3}, the same for the query vectors (A) and the
+// keys (B); value n-tile 4 blk + j holds n = lane group r as dim 32 blk + 4r + j.
+
+constexpr float kInvSqrtD = 0.0883883476483184405f;  // 1 / sqrt(128), correctly rounded
+
+__device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                        uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Two codes of `u` (four codes with their sign bits flipped, i.e. code + 128
+// as unsigned bytes) as binary16x2, exactly: `sel` moves the two bytes into
+// the low mantissa bytes of 1024.0 (0x64 high bytes), giving 1024 + code + 128,
+// and subtracting 1152 leaves the code.  sel 0x4140: bytes 0 and 1; 0x4342:
+// bytes 2 and 3 (the lower-numbered byte in the low half).
+__device__ __forceinline__ uint32_t codes_f16x2(uint32_t u, uint32_t sel) {
+    const uint32_t h = __byte_perm(u, 0x64646464u, sel);
+    const __half2 r = __hsub2(*reinterpret_cast<const __half2*>(&h),
+                              __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480)));
+    return *reinterpret_cast<const uint32_t*>(&r);
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    const __half2 r = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&r);
+}
+
+// Binary16 rounding of x and of what it leaves: hi + lo carries ~22 bits of x.
+__device__ __forceinline__ void split_f16x2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+    const __half2 h = __floats2half2_rn(x0, x1);
+    const float2 hf = __half22float2(h);
+    hi = *reinterpret_cast<const uint32_t*>(&h);
+    lo = pack_f16x2(x0 - hf.x, x1 - hf.y);
+}
+
+// 2^e for -126 <= e <= 127, exactly.
+__device__ __forceinline__ float pow2i(int e) { return __uint_as_float(static_cast<uint32_t>(e + 127) << 23); }
+
+// floor(log2 x) for a positive normal x.
+__device__ __forceinline__ int ilog2f(float x) {
+    return static_cast<int>((__float_as_uint(x) >> 23) & 0xffu) - 127;
+}
+
+__device__ __forceinline__ float scale_of(uint2 w, int blk) {
+    const uint32_t v = blk < 2 ? w.x : w.y;
+    return half_bits(static_cast<uint16_t>((blk & 1) ? (v >> 16) : (v & 0xffffu)));
+}
+
+__global__ void __launch_bounds__(kThreads) attn_split_tc_kernel(const AttnArgs a) {
+    __shared__ float qs[kQB][kD];
+    __shared__ int q_row[kQB], q_head[kQB], q_pos[kQB];
+    __shared__ float wm[kWarps][kQB], wl[kWarps][kQB];
+    __shared__ float wacc[kWarps][kQB][kD];
+    __shared__ float wmax[kWarps];
+    const int s = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int gr = lane >> 2, qc = lane & 3;  // lane group (row / n index) and position in the quad
+    const int group = a.Hq / a.Hkv;
+    const int L = __ldg(a.seq_len + b);
+    if (L > a.splits * a.chunk || L > a.max_pages * a.T) {
+        if (threadIdx.x == 0 && s == 0 && h == 0) atomicExch(a.err, kErrBadTable);
+        return;
+    }
+    const int t0 = s * a.chunk;
+    const int t1 = min(L, t0 + a.chunk);
+    int next_row = 0;
+    for (;;) {
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            int n = 0;
+            int i = next_row;
+            for (; i < a.rows && n + group <= kQB; ++i) {
+                if (__ldg(a.row_seq + i) != b) continue;
+                const int pos = __ldg(a.row_pos + i);
+                const bool ok = pos >= 0 && pos < L;
+                if (!ok) atomicExch(a.err, kErrBadTable);
+                for (int hh = 0; hh < group; ++hh) {
+                    q_row[n] = i;
+                    q_head[n] = h * group + hh;
+                    q_pos[n] = ok ? pos : -1;
+                    ++n;
+                }
+            }
+            next_row = i;
+            for (int j = n; j < kQB; ++j) {
+                q_row[j] = -1;
+                q_head[j] = 0;
+                q_pos[j] = -1;
+            }
+        }
+        __syncthreads();
+        int qn = 0;
+        for (int j = 0; j < kQB; ++j) qn += q_row[j] >= 0 ? 1 : 0;
+        if (qn == 0) break;
+        float qmax = 0.f;
+        for (int e = threadIdx.x; e < kQB * kD; e += kThreads) {
+            const int j = e / kD, d = e % kD;
+            const float v = q_row[j] >= 0
+                                ? bf16_bits(__ldg(a.q + (static_cast<long>(q_row[j]) * a.Hq + q_head[j]) * kD + d))
+                                : 0.f;
+            qs[j][d] = v;
+            qmax = fmaxf(qmax, fabsf(v));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, o));
+        if (lane == 0) wmax[warp] = qmax;
+        __syncthreads();
+        qmax = fmaxf(fmaxf(wmax[0], wmax[1]), fmaxf(wmax[2], wmax[3]));
+        // 2^eq puts the largest query value in [2^14, 2^15); zero or subnormal
+        // maxima (nothing to scale) keep eq = 0
+        const int eq = qmax >= 1.17549435e-38f ? max(-100, min(100, 14 - ilog2f(qmax))) : 0;
+        const float qsc = ldexpf(1.f, eq);
+        const float ssc = ldexpf(kInvSqrtD, -eq);  // undoes 2^eq and applies 1 / sqrt(D)
+        uint32_t qa[8][4];
+#pragma unroll
+        for (int blk = 0; blk < 4; ++blk)
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int d0 = 32 * blk + 8 * qc + 4 * hh;
+                uint32_t* f = qa[2 * blk + hh];
+                f[0] = pack_f16x2(qs[gr][d0] * qsc, qs[gr][d0 + 1] * qsc);
+                f[1] = pack_f16x2(qs[gr + 8][d0] * qsc, qs[gr + 8][d0 + 1] * qsc);
+                f[2] = pack_f16x2(qs[gr][d0 + 2] * qsc, qs[gr][d0 + 3] * qsc);
+                f[3] = pack_f16x2(qs[gr + 8][d0 + 2] * qsc, qs[gr + 8][d0 + 3] * qsc);
+            }
+        const int qp0 = q_pos[gr], qp1 = q_pos[gr + 8];
+        float o[16][4];
+#pragma unroll
+        for (int n = 0; n < 16; ++n)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) o[n][e] = 0.f;
+        float m0 = -INFINITY, m1 = -INFINITY;  // running maxima of rows gr and gr + 8
+        float l0 = 0.f, l1 = 0.f;              // this lane's share of the running sums
+        int ev = 64;                           // O holds 2^ev times the weighted values (64: not set yet)
+        for (int base = t0 + 16 * warp; base < t1; base += 16 * kWarps) {
+            // pool rows of positions base + lane (lanes 0 .. 15), then each
+            // lane's positions: keys (n = gr of both n-tiles) and the C
+            // fragment / value positions base + 2qc + {0, 1} and base + 8 + 2qc + {0, 1}
+            long myrow = -1;
+            if (lane < 16 && base + lane < t1) {
+                myrow = token_row(a, b, h, base + lane);
+                if (myrow < 0) atomicExch(a.err, kErrBadTable);
+            }
+            const long rk0 = __shfl_sync(0xffffffffu, myrow, gr);
+            const long rk1 = __shfl_sync(0xffffffffu, myrow, 8 + gr);
+            long rv[4];
+            rv[0] = __shfl_sync(0xffffffffu, myrow, 2 * qc);
+            rv[1] = __shfl_sync(0xffffffffu, myrow, 2 * qc + 1);
+            rv[2] = __shfl_sync(0xffffffffu, myrow, 8 + 2 * qc);
+            rv[3] = __shfl_sync(0xffffffffu, myrow, 9 + 2 * qc);
+            uint2 kw[2][4], ksc[4], vsc[4];
+            uint32_t vw[4][4];
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                const long rk = nt ? rk1 : rk0;
+#pragma unroll
+                for (int blk = 0; blk < 4; ++blk)
+                    kw[nt][blk] = rk >= 0 ? __ldg(reinterpret_cast<const uint2*>(a.kc + rk * kD + 32 * blk + 8 * qc))
+                                          : make_uint2(0u, 0u);
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const bool ok = rv[j] >= 0;
+                ksc[j] = ok ? __ldg(reinterpret_cast<const uint2*>(a.kd + rv[j] * (kD / 32))) : make_uint2(0u, 0u);
+                vsc[j] = ok ? __ldg(reinterpret_cast<const uint2*>(a.vd + rv[j] * (kD / 32))) : make_uint2(0u, 0u);
+#pragma unroll
+                for (int blk = 0; blk < 4; ++blk)
+                    vw[j][blk] = ok ? __ldg(reinterpret_cast<const uint32_t*>(a.vc + rv[j] * kD + 32 * blk + 4 * gr))
+                                    : 0u;
+            }
+            // scores: sv[nt][i] = C fragment element i of n-tile nt (rows gr, gr, gr + 8, gr + 8;
+            // positions base + 8 nt + 2 qc + {0, 1, 0, 1})
+            float sv[2][4];
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) sv[nt][e] = 0.f;
+#pragma unroll
+                for (int blk = 0; blk < 4; ++blk) {
+                    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                    const uint32_t u0 = kw[nt][blk].x ^ 0x80808080u, u1 = kw[nt][blk].y ^ 0x80808080u;
+                    mma_f16(acc, qa[2 * blk], codes_f16x2(u0, 0x4140), codes_f16x2(u0, 0x4342));
+                    mma_f16(acc, qa[2 * blk + 1], codes_f16x2(u1, 0x4140), codes_f16x2(u1, 0x4342));
+                    const float d0 = scale_of(ksc[2 * nt], blk), d1 = scale_of(ksc[2 * nt + 1], blk);
+                    sv[nt][0] = fmaf(acc[0], d0, sv[nt][0]);
+                    sv[nt][1] = fmaf(acc[1], d1, sv[nt][1]);
+                    sv[nt][2] = fmaf(acc[2], d0, sv[nt][2]);
+                    sv[nt][3] = fmaf(acc[3], d1, sv[nt][3]);
+                }
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int j = 2 * nt + (e & 1);                  // which of rv[]
+                    const int t = base + 8 * nt + 2 * qc + (e & 1);  // its position
+                    const int qp = e < 2 ? qp0 : qp1;
+                    sv[nt][e] = (rv[j] >= 0 && t <= qp) ? sv[nt][e] * ssc : -INFINITY;
+                }
+            }
+            // online softmax per row: maxima over the chunk's 16 positions (own
+            // four values, then the quad), rescale of the running state
+            float mx0 = fmaxf(fmaxf(sv[0][0], sv[0][1]), fmaxf(sv[1][0], sv[1][1]));
+            float mx1 = fmaxf(fmaxf(sv[0][2], sv[0][3]), fmaxf(sv[1][2], sv[1][3]));
+#pragma unroll
+            for (int o2 = 1; o2 <= 2; o2 <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o2));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o2));
+            }
+            const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+            const float k0 = mn0 == -INFINITY ? 1.f : __expf(m0 - mn0);
+            const float k1 = mn1 == -INFINITY ? 1.f : __expf(m1 - mn1);
+            m0 = mn0;
+            m1 = mn1;
+            float p[2][4];
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float mr = e < 2 ? mn0 : mn1;
+                    p[nt][e] = sv[nt][e] == -INFINITY ? 0.f : __expf(sv[nt][e] - mr);
+                }
+            l0 = l0 * k0 + (p[0][0] + p[0][1]) + (p[1][0] + p[1][1]);
+            l1 = l1 * k1 + (p[0][2] + p[0][3]) + (p[1][2] + p[1][3]);
+            // the chunk's largest value scale sets 2^ev (only ever lowered; O follows)
+            float dmax = 0.f;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+#pragma unroll
+                for (int blk = 0; blk < 4; ++blk) dmax = fmaxf(dmax, fabsf(scale_of(vsc[j], blk)));
+#pragma unroll
+            for (int o2 = 1; o2 <= 2; o2 <<= 1) dmax = fmaxf(dmax, __shfl_xor_sync(0xffffffffu, dmax, o2));
+            // binary16 scales are at least 2^-24 when not zero
+            const int ev_c = dmax > 0.f ? 14 - ilog2f(dmax) : 64;
+            float r0 = k0, r1 = k1;
+            if (ev_c < ev) {
+                const float f = pow2i(max(ev_c - ev, -126));
+                r0 *= f;
+                r1 *= f;
+                ev = ev_c;
+            }
+#pragma unroll
+            for (int n = 0; n < 16; ++n) {
+                o[n][0] *= r0;
+                o[n][1] *= r0;
+                o[n][2] *= r1;
+                o[n][3] *= r1;
+            }
+            const float evs = pow2i(min(ev, 127));
+            // values, one 32-dim block at a time
+#pragma unroll
+            for (int blk = 0; blk < 4; ++blk) {
+                float ds[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) ds[j] = scale_of(vsc[j], blk) * evs;
+                // A: rows gr / gr + 8, k = 2qc, 2qc + 1 (positions rv[0], rv[1]) and
+                // k = 2qc + 8, 2qc + 9 (rv[2], rv[3])
+                uint32_t ah[4], al[4];
+                split_f16x2(p[0][0] * ds[0], p[0][1] * ds[1], ah[0], al[0]);
+                split_f16x2(p[0][2] * ds[0], p[0][3] * ds[1], ah[1], al[1]);
+                split_f16x2(p[1][0] * ds[2], p[1][1] * ds[3], ah[2], al[2]);
+                split_f16x2(p[1][2] * ds[2], p[1][3] * ds[3], ah[3], al[3]);
+                // B: the four positions' codes at dims 32 blk + 4 gr + j, transposed
+                // so that each 16-bit half holds two positions at one dim
+                const uint32_t u0 = vw[0][blk] ^ 0x80808080u, u1 = vw[1][blk] ^ 0x80808080u;
+                const uint32_t u2 = vw[2][blk] ^ 0x80808080u, u3 = vw[3][blk] ^ 0x80808080u;
+                const uint32_t t01a = __byte_perm(u0, u1, 0x5140), t01b = __byte_perm(u0, u1, 0x7362);
+                const uint32_t t23a = __byte_perm(u2, u3, 0x5140), t23b = __byte_perm(u2, u3, 0x7362);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint32_t lo = j < 2 ? t01a : t01b, hi = j < 2 ? t23a : t23b;
+                    const uint32_t sel = (j & 1) ? 0x4342u : 0x4140u;
+                    const uint32_t b0 = codes_f16x2(lo, sel), b1 = codes_f16x2(hi, sel);
+                    mma_f16(o[4 * blk + j], ah, b0, b1);
+                    mma_f16(o[4 * blk + j], al, b0, b1);
+                }
+            }
+        }
+        // this warp's state: maxima (uniform in the quad), sums over the quad,
+        // O without its 2^ev
+#pragma unroll
+        for (int o2 = 1; o2 <= 2; o2 <<= 1) {
+            l0 += __shfl_xor_sync(0xffffffffu, l0, o2);
+            l1 += __shfl_xor_sync(0xffffffffu, l1, o2);
+        }
+        if (qc == 0) {
+            wm[warp][gr] = m0;
+            wm[warp][gr + 8] = m1;
+            wl[warp][gr] = l0;
+            wl[warp][gr + 8] = l1;
+        }
+        const float inv = pow2i(-min(ev, 126));
+#pragma unroll
+        for (int blk = 0; blk < 4; ++blk)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int d = 32 * blk + 8 * qc + j;
+                wacc[warp][gr][d] = o[4 * blk + j][0] * inv;
+                wacc[warp][gr][d + 4] = o[4 * blk + j][1] * inv;
+                wacc[warp][gr + 8][d] = o[4 * blk + j][2] * inv;
+                wacc[warp][gr + 8][d + 4] = o[4 * blk + j][3] * inv;
+            }
+        __syncthreads();
+        // merge the warps in warp order (as the CUDA-core kernel)
+        for (int e = threadIdx.x; e < kQB * kD; e += kThreads) {
+            const int j = e / kD, d = e % kD;
+            if (q_row[j] < 0) continue;
+            float mt = -INFINITY;
+            for (int w = 0; w < kWarps; ++w) mt = fmaxf(mt, wm[w][j]);
+            float lt = 0.f, at = 0.f;
+            for (int w = 0; w < kWarps; ++w) {
+                const float f = wm[w][j] == -INFINITY ? 0.f : expf(wm[w][j] - mt);
+                lt += f * wl[w][j];
+                at += f * wacc[w][j][d];
+            }
+            float* dst = a.part + ((static_cast<long>(q_row[j]) * a.Hq + q_head[j]) * a.splits + s) * (2 + kD);
+            if (d == 0) {
+                dst[0] = mt;
+                dst[1] = lt;
+            }
+            dst[2 + d] = at;
+        }
+    }
+}
+
 // out[i][h] = (sum over slices of e^(m_s - m) acc_s) / (sum of e^(m_s - m) l_s), slices in order.
 __global__ void __launch_bounds__(kD) attn_combine_kernel(const float* part, int splits, int Hq,
                                                           float* out) {
@@ -258,12 +607,18 @@ size_t wq_paged_attention_workspace_bytes(int rows, int Hq, int max_seq_len) {
     return wq::kWsHeader + static_cast<size_t>(rows) * Hq * splits * (2 + kD) * sizeof(float);
 }
 
-wq_status_t wq_paged_attention(const uint16_t* q, const int8_t* k_codes, const uint16_t* k_scales,
-                               const int8_t* v_codes, const uint16_t* v_scales,
-                               const int* page_table, int max_pages, const int* seq_len, int B,
-                               const int* row_seq, const int* row_pos, int rows, int max_seq_len,
-                               int Hq, int Hkv, int D, int T, int pages, float* out,
-                               void* workspace, size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Checks, workspace layout and the two launches; tensor_cores selects the
+// split kernel (the CUDA-core one stays as an independent cross-check).
+wq_status_t paged_attention(const uint16_t* q, const int8_t* k_codes, const uint16_t* k_scales,
+                            const int8_t* v_codes, const uint16_t* v_scales, const int* page_table,
+                            int max_pages, const int* seq_len, int B, const int* row_seq,
+                            const int* row_pos, int rows, int max_seq_len, int Hq, int Hkv, int D,
+                            int T, int pages, float* out, void* workspace, size_t workspace_bytes,
+                            void* stream, bool tensor_cores) {
     if (D != kD || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || Hq / Hkv > kQB || T <= 0 ||
         pages <= 0 || B <= 0 || max_pages <= 0 || rows < 0 || max_seq_len <= 0 ||
         max_seq_len > max_pages * T)
@@ -272,7 +627,8 @@ wq_status_t wq_paged_attention(const uint16_t* q, const int8_t* k_codes, const u
     if (!q || !k_codes || !k_scales || !v_codes || !v_scales || !page_table || !seq_len ||
         !row_seq || !row_pos || !out || !workspace)
         return WQ_ERR_INVALID_ARG;
-    if (!aligned(k_codes, 16) || !aligned(v_codes, 16) || !aligned(out, 4) ||
+    if (!aligned(k_codes, 16) || !aligned(v_codes, 16) || !aligned(k_scales, 8) ||
+        !aligned(v_scales, 8) || !aligned(out, 4) ||
         workspace_bytes < wq_paged_attention_workspace_bytes(rows, Hq, max_seq_len) ||
         !aligned(workspace, 16))
         return WQ_ERR_INVALID_ARG;
@@ -301,10 +657,40 @@ wq_status_t wq_paged_attention(const uint16_t* q, const int8_t* k_codes, const u
     // never read, and empty slices write m = -inf, l = 0
     cudaError_t e = cudaMemsetAsync(a.part, 0, static_cast<size_t>(rows) * Hq * a.splits * (2 + kD) * sizeof(float), s);
     if (e != cudaSuccess) return WQ_ERR_CUDA;
-    attn_split_kernel<<<dim3(a.splits, Hkv, B), kThreads, 0, s>>>(a);
+    if (tensor_cores)
+        attn_split_tc_kernel<<<dim3(a.splits, Hkv, B), kThreads, 0, s>>>(a);
+    else
+        attn_split_kernel<<<dim3(a.splits, Hkv, B), kThreads, 0, s>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return WQ_ERR_CUDA;
     attn_combine_kernel<<<static_cast<unsigned>(rows * Hq), kD, 0, s>>>(a.part, a.splits, Hq, out);
     return cudaGetLastError() == cudaSuccess ? WQ_OK : WQ_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+wq_status_t wq_paged_attention(const uint16_t* q, const int8_t* k_codes, const uint16_t* k_scales,
+                               const int8_t* v_codes, const uint16_t* v_scales,
+                               const int* page_table, int max_pages, const int* seq_len, int B,
+                               const int* row_seq, const int* row_pos, int rows, int max_seq_len,
+                               int Hq, int Hkv, int D, int T, int pages, float* out,
+                               void* workspace, size_t workspace_bytes, void* stream) {
+    return paged_attention(q, k_codes, k_scales, v_codes, v_scales, page_table, max_pages, seq_len,
+                           B, row_seq, row_pos, rows, max_seq_len, Hq, Hkv, D, T, pages, out,
+                           workspace, workspace_bytes, stream, true);
+}
+
+// The same on the CUDA cores (fp32 FMA throughout): not part of include/wq.h;
+// the tests compare the two kernels with each other and with the oracle.
+wq_status_t wq_internal_paged_attention_cuda_cores(
+    const uint16_t* q, const int8_t* k_codes, const uint16_t* k_scales, const int8_t* v_codes,
+    const uint16_t* v_scales, const int* page_table, int max_pages, const int* seq_len, int B,
+    const int* row_seq, const int* row_pos, int rows, int max_seq_len, int Hq, int Hkv, int D,
+    int T, int pages, float* out, void* workspace, size_t workspace_bytes, void* stream) {
+    return paged_attention(q, k_codes, k_scales, v_codes, v_scales, page_table, max_pages, seq_len,
+                           B, row_seq, row_pos, rows, max_seq_len, Hq, Hkv, D, T, pages, out,
+                           workspace, workspace_bytes, stream, false);
 }
 
 }  // extern "C"
