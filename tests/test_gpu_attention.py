@@ -144,3 +144,29 @@ def test_bad_page_is_reported():
     ws = torch.zeros(n, dtype=torch.uint8, device=dev())
     _run(d, workspace=ws)
     assert int(ws[:4].view(torch.int32).item()) == 2
+
+
+# The workload the benchmark times: four agents x 32768 positions of their own
+# sequences (a 4096-token prefix stored once and shared), three query rows each,
+# 40 query heads over 8 key/value heads, 64-token pages.
+BENCH_CASE = synth.PagedAttention("bench", (32768,) * 4, 3, 40, 8, 128, 64, 31,
+                                  shared_prefix=4096)
+
+
+def test_bench_workload_sampled_rows():
+    # full size, as timed; the oracle computes sampled rows from a host copy of
+    # the device pool (the device generator gives the numpy generator's bits)
+    import weight_only_bit_wq_gb300 as wq
+    p = BENCH_CASE
+    t = synth.gen_paged_attention_torch(p, dev())
+    out = wq.wq_paged_attention(t["q"], t["kc"], t["kd"], t["vc"], t["vd"], t["page_table"],
+                                t["seq_len"], t["row_seq"], t["row_pos"], max(p.seq_lens))
+    torch.cuda.synchronize()
+    got = out.cpu().numpy()
+    host = {k: v.cpu().numpy() for k, v in t.items()}
+    rows = np.array([0, 4, 8, 11])  # first and last rows, each agent once
+    ref = oracle.paged_attention_f64(host["q"][rows].view(np.uint16), host["kc"],
+                                     host["kd"].view(np.uint16), host["vc"],
+                                     host["vd"].view(np.uint16), host["page_table"],
+                                     host["seq_len"], host["row_seq"][rows], host["row_pos"][rows])
+    assert np.abs(got[rows] - ref).max() <= TOL * np.abs(ref).max()
