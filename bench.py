@@ -462,7 +462,7 @@ def run_attention(device, stream, peak, steps, warmup):
     B, max_pages = t["page_table"].shape
     msl = max(p.seq_lens)
     out = torch.empty((rows, Hq, D), dtype=torch.float32, device=device)
-    n = int(wq._lib().wq_paged_attention_workspace_bytes(rows, Hq, msl))
+    n = int(wq._lib().wq_paged_attention_workspace_bytes(rows, Hq, Hkv, B, msl))
     ws = torch.zeros(max(n, 256), dtype=torch.uint8, device=device)
     lib = wq._lib()
     cc = lib.wq_internal_paged_attention_cuda_cores

@@ -284,13 +284,14 @@ void wq_step_graph_destroy(wq_step_graph_t graph);
  * seq_len int32 [B]; row_seq, row_pos int32 [rows]; out fp32 [rows][Hq][D].
  * D = 128; Hq a multiple of Hkv with Hq / Hkv <= 16; max_seq_len (host) bounds
  * every seq_len and max_pages * T >= max_seq_len.  workspace: at least
- * wq_paged_attention_workspace_bytes(rows, Hq, max_seq_len) bytes, 16-byte
+ * wq_paged_attention_workspace_bytes(rows, Hq, Hkv, B, max_seq_len) bytes (the
+ * slices per sequence follow the current device's SM count), 16-byte
  * aligned, its first word zero; a page index outside the pool, a position
  * past its sequence or a sequence longer than max_seq_len sets that word to 2
  * (the affected rows read nothing).  Rows whose row_seq is not in [0, B)
  * produce zeros.  Deterministic: the same inputs give the same bits.
  */
-size_t wq_paged_attention_workspace_bytes(int rows, int Hq, int max_seq_len);
+size_t wq_paged_attention_workspace_bytes(int rows, int Hq, int Hkv, int B, int max_seq_len);
 wq_status_t wq_paged_attention(const uint16_t* q, const int8_t* k_codes, const uint16_t* k_scales,
                                const int8_t* v_codes, const uint16_t* v_scales,
                                const int* page_table, int max_pages, const int* seq_len, int B,

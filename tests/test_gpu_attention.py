@@ -57,7 +57,7 @@ def _run(d, max_seq_len=None, workspace=None, cuda_cores=False):
         pages, Hkv, T, _ = t["kc"].shape
         B, max_pages = t["page_table"].shape
         out = torch.empty((rows, Hq, D), dtype=torch.float32, device=dev())
-        n = int(wq._lib().wq_paged_attention_workspace_bytes(rows, Hq, msl))
+        n = int(wq._lib().wq_paged_attention_workspace_bytes(rows, Hq, Hkv, B, msl))
         ws = torch.zeros(max(n, 256), dtype=torch.uint8, device=dev())
         p = lambda x: ctypes.c_void_p(x.data_ptr())
         st = _cuda_cores(wq)(p(t["q"]), p(t["kc"]), p(t["kd"]), p(t["vc"]), p(t["vd"]),
@@ -139,8 +139,8 @@ def test_bad_page_is_reported():
     d = dict(d)
     d["page_table"] = d["page_table"].copy()
     d["page_table"][1, 2] = d["kc"].shape[0] + 5  # outside the pool
-    n = int(wq._lib().wq_paged_attention_workspace_bytes(len(d["row_seq"]), p.Hq,
-                                                          int(d["seq_len"].max())))
+    n = int(wq._lib().wq_paged_attention_workspace_bytes(len(d["row_seq"]), p.Hq, p.Hkv,
+                                                          len(p.seq_lens), int(d["seq_len"].max())))
     ws = torch.zeros(n, dtype=torch.uint8, device=dev())
     _run(d, workspace=ws)
     assert int(ws[:4].view(torch.int32).item()) == 2

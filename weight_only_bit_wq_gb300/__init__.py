@@ -75,7 +75,7 @@ def _lib() -> ctypes.CDLL:
             "wq_gemm": ([P, P, P, P, P, I, I, I, I, I, P, S, P], I),
             "wq_gemm_swiglu": ([P, P, P, P, P, I, I, I, I, I, P, S, P], I),
             "wq_check_workspace": ([P, P], I),
-            "wq_paged_attention_workspace_bytes": ([I, I, I], S),
+            "wq_paged_attention_workspace_bytes": ([I, I, I, I, I], S),
             "wq_paged_attention": ([P, P, P, P, P, P, I, P, I, P, P, I, I, I, I, I, I, I, P, P, S, P], I),
             "wq_step_workspace_bytes": ([P, I, ctypes.c_uint], S),
             "wq_step_run": ([P, I, P, S, P], I),
@@ -208,7 +208,7 @@ def wq_paged_attention(q, kc, kd, vc, vd, page_table, seq_len, row_seq, row_pos,
     if out is None:
         out = torch.empty((rows, Hq, D), dtype=torch.float32, device=q.device)
     if workspace is None:
-        n = int(_lib().wq_paged_attention_workspace_bytes(rows, Hq, max_seq_len))
+        n = int(_lib().wq_paged_attention_workspace_bytes(rows, Hq, Hkv, B, max_seq_len))
         workspace = torch.zeros(max(n, 256), dtype=torch.uint8, device=q.device)
     nbytes = workspace.numel() * workspace.element_size()
     _check(_lib().wq_paged_attention(_ptr(q), _ptr(kc), _ptr(kd), _ptr(vc), _ptr(vd),

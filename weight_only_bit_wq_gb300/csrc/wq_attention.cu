@@ -583,15 +583,21 @@ __global__ void __launch_bounds__(kD) attn_combine_kernel(const float* part, int
     out[vec * kD + d] = lt > 0.f ? at / lt : 0.f;
 }
 
-int splits_for(int max_seq_len, int* chunk) {
-    // slices of at least 512 positions, at most 64 per sequence
-    int splits = (max_seq_len + 511) / 512;
-    if (splits > 64) splits = 64;
-    if (splits < 1) splits = 1;
-    int c = (max_seq_len + splits - 1) / splits;
+// Slices per sequence: about four CTAs per SM over the whole grid (two waves
+// at two resident CTAs per SM), no slice under 256 positions, at most 64; the
+// slice length rounded up to 128 positions (whole iterations of the CUDA-core
+// kernel's four warps of 32 positions).
+int splits_for(int max_seq_len, int B, int Hkv, int sms, int* chunk) {
+    const long long heads = static_cast<long long>(B) * Hkv;
+    long long want = 4LL * sms / (heads > 0 ? heads : 1);
+    const long long most = (static_cast<long long>(max_seq_len) + 255) / 256;
+    if (want > most) want = most;
+    if (want > 64) want = 64;
+    if (want < 1) want = 1;
+    long long c = (max_seq_len + want - 1) / want;
     c = (c + 127) / 128 * 128;
-    *chunk = c;
-    return splits;
+    *chunk = static_cast<int>(c);
+    return static_cast<int>((max_seq_len + c - 1) / c);
 }
 
 bool aligned(const void* p, size_t n) { return reinterpret_cast<uintptr_t>(p) % n == 0; }
@@ -600,10 +606,12 @@ bool aligned(const void* p, size_t n) { return reinterpret_cast<uintptr_t>(p) % 
 
 extern "C" {
 
-size_t wq_paged_attention_workspace_bytes(int rows, int Hq, int max_seq_len) {
-    if (rows < 0 || Hq <= 0 || max_seq_len <= 0) return 0;
+size_t wq_paged_attention_workspace_bytes(int rows, int Hq, int Hkv, int B, int max_seq_len) {
+    if (rows < 0 || Hq <= 0 || Hkv <= 0 || B <= 0 || max_seq_len <= 0) return 0;
+    int sms = 0;
+    if (wq::host_sm_count(&sms) != WQ_OK) return 0;
     int chunk = 0;
-    const int splits = splits_for(max_seq_len, &chunk);
+    const int splits = splits_for(max_seq_len, B, Hkv, sms, &chunk);
     return wq::kWsHeader + static_cast<size_t>(rows) * Hq * splits * (2 + kD) * sizeof(float);
 }
 
@@ -629,7 +637,7 @@ wq_status_t paged_attention(const uint16_t* q, const int8_t* k_codes, const uint
         return WQ_ERR_INVALID_ARG;
     if (!aligned(k_codes, 16) || !aligned(v_codes, 16) || !aligned(k_scales, 8) ||
         !aligned(v_scales, 8) || !aligned(out, 4) ||
-        workspace_bytes < wq_paged_attention_workspace_bytes(rows, Hq, max_seq_len) ||
+        workspace_bytes < wq_paged_attention_workspace_bytes(rows, Hq, Hkv, B, max_seq_len) ||
         !aligned(workspace, 16))
         return WQ_ERR_INVALID_ARG;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -650,7 +658,9 @@ wq_status_t paged_attention(const uint16_t* q, const int8_t* k_codes, const uint
     a.Hkv = Hkv;
     a.T = T;
     a.pages = pages;
-    a.splits = splits_for(max_seq_len, &a.chunk);
+    int sms = 0;
+    if (wq_status_t st = wq::host_sm_count(&sms)) return st;
+    a.splits = splits_for(max_seq_len, B, Hkv, sms, &a.chunk);
     a.err = static_cast<int*>(workspace);
     a.part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + wq::kWsHeader);
     // every (row, head, slice) state is written: rows of other sequences are
