@@ -285,7 +285,7 @@ void wq_step_graph_destroy(wq_step_graph_t graph);
  * D = 128; Hq a multiple of Hkv with Hq / Hkv <= 16; max_seq_len (host) bounds
  * every seq_len and max_pages * T >= max_seq_len.  workspace: at least
  * wq_paged_attention_workspace_bytes(rows, Hq, Hkv, B, max_seq_len) bytes (the
- * slices per sequence follow the current device's SM count), 16-byte
+ * slices per sequence follow the current device's size), 16-byte
  * aligned, its first word zero; a page index outside the pool, a position
  * past its sequence or a sequence longer than max_seq_len sets that word to 2
  * (the affected rows read nothing).  Rows whose row_seq is not in [0, B)

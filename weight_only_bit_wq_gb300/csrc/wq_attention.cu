@@ -27,6 +27,7 @@
 
 #include "wq.h"
 #include "wq_internal.h"
+#include "wq_ptx.cuh"
 
 namespace {
 
@@ -291,12 +292,25 @@ __device__ __forceinline__ float scale_of(uint2 w, int blk) {
     return half_bits(static_cast<uint16_t>((blk & 1) ? (v >> 16) : (v & 0xffffu)));
 }
 
+// A warp's copy stage: 16 positions of K codes and of V codes (128-byte rows
+// whose 16-byte pieces are stored XOR-swizzled by the row, so that the lanes'
+// fragment reads hit distinct banks), then their K and V scale quadruples.
+constexpr int kOffK = 0, kOffV = 16 * kD, kOffKS = 32 * kD, kOffVS = 32 * kD + 16 * 8;
+constexpr int kStageBytes = 32 * kD + 2 * 16 * 8;
+constexpr int kRingBytes = kWarps * 2 * kStageBytes;
+constexpr int kWaccBytes = kWarps * kQB * kD * 4;
+constexpr int kSbufBytes = kRingBytes > kWaccBytes ? kRingBytes : kWaccBytes;
+__device__ __forceinline__ int swz(int piece, int row) { return piece ^ (row & 7); }
+
 __global__ void __launch_bounds__(kThreads) attn_split_tc_kernel(const AttnArgs a) {
     __shared__ float qs[kQB][kD];
     __shared__ int q_row[kQB], q_head[kQB], q_pos[kQB];
     __shared__ float wm[kWarps][kQB], wl[kWarps][kQB];
-    __shared__ float wacc[kWarps][kQB][kD];
     __shared__ float wmax[kWarps];
+    // each warp's two-stage copy ring during the position loop, then the
+    // warps' weighted values for the merge
+    __shared__ __align__(16) unsigned char sbuf[kSbufBytes];
+    float(*wacc)[kQB][kD] = reinterpret_cast<float(*)[kQB][kD]>(sbuf);
     const int s = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int gr = lane >> 2, qc = lane & 3;  // lane group (row / n index) and position in the quad
@@ -377,53 +391,83 @@ __global__ void __launch_bounds__(kThreads) attn_split_tc_kernel(const AttnArgs 
         float m0 = -INFINITY, m1 = -INFINITY;  // running maxima of rows gr and gr + 8
         float l0 = 0.f, l1 = 0.f;              // this lane's share of the running sums
         int ev = 64;                           // O holds 2^ev times the weighted values (64: not set yet)
-        for (int base = t0 + 16 * warp; base < t1; base += 16 * kWarps) {
-            // pool rows of positions base + lane (lanes 0 .. 15), then each
-            // lane's positions: keys (n = gr of both n-tiles) and the C
-            // fragment / value positions base + 2qc + {0, 1} and base + 8 + 2qc + {0, 1}
+        unsigned char* const ring = sbuf + warp * 2 * kStageBytes;
+        // Copies one chunk (positions base .. base + 15) into stage st: pool
+        // rows of the positions from lanes 0 .. 15, then four 16-byte pieces of
+        // K and of V codes per lane (zero-filled for positions outside the
+        // slice or the pool) and one 8-byte scale quadruple.  Returns the
+        // chunk's readable positions as a bit mask.
+        auto issue = [&](int base, int st) -> unsigned {
             long myrow = -1;
             if (lane < 16 && base + lane < t1) {
                 myrow = token_row(a, b, h, base + lane);
                 if (myrow < 0) atomicExch(a.err, kErrBadTable);
             }
-            const long rk0 = __shfl_sync(0xffffffffu, myrow, gr);
-            const long rk1 = __shfl_sync(0xffffffffu, myrow, 8 + gr);
-            long rv[4];
-            rv[0] = __shfl_sync(0xffffffffu, myrow, 2 * qc);
-            rv[1] = __shfl_sync(0xffffffffu, myrow, 2 * qc + 1);
-            rv[2] = __shfl_sync(0xffffffffu, myrow, 8 + 2 * qc);
-            rv[3] = __shfl_sync(0xffffffffu, myrow, 9 + 2 * qc);
-            uint2 kw[2][4], ksc[4], vsc[4];
-            uint32_t vw[4][4];
+            const unsigned vmask = __ballot_sync(0xffffffffu, myrow >= 0);
+            const uint32_t sb = wq::smem_addr(ring + st * kStageBytes);
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                const long rk = nt ? rk1 : rk0;
-#pragma unroll
-                for (int blk = 0; blk < 4; ++blk)
-                    kw[nt][blk] = rk >= 0 ? __ldg(reinterpret_cast<const uint2*>(a.kc + rk * kD + 32 * blk + 8 * qc))
-                                          : make_uint2(0u, 0u);
+            for (int i = 0; i < 4; ++i) {
+                const int c = lane + 32 * i;  // piece c: position c / 8, bytes 16 (c % 8) ..
+                const int r = c >> 3, p = c & 7;
+                const long row = __shfl_sync(0xffffffffu, myrow, r);
+                const uint32_t off = static_cast<uint32_t>(r * kD + (swz(p, r) << 4));
+                const long src = row >= 0 ? row * kD + 16 * p : 0;
+                const uint32_t n = row >= 0 ? 16u : 0u;
+                wq::cp_async_n<16>(sb + kOffK + off, a.kc + src, n);
+                wq::cp_async_n<16>(sb + kOffV + off, a.vc + src, n);
             }
+            {
+                const int r = lane & 15;
+                const long row = __shfl_sync(0xffffffffu, myrow, r);
+                const uint16_t* src = (lane < 16 ? a.kd : a.vd) + (row >= 0 ? row * (kD / 32) : 0);
+                wq::cp_async_n<8>(sb + (lane < 16 ? kOffKS : kOffVS) + 8 * r, src, row >= 0 ? 8u : 0u);
+            }
+            wq::cp_async_commit();
+            return vmask;
+        };
+        const int step = 16 * kWarps;
+        int base = t0 + 16 * warp;
+        unsigned vm_cur = base < t1 ? issue(base, 0) : 0u;
+        for (int it = 0; base < t1; ++it, base += step) {
+            const int st = it & 1;
+            // the next chunk's copies fly while this one is computed
+            unsigned vm_next = 0u;
+            if (base + step < t1)
+                vm_next = issue(base + step, st ^ 1);
+            else
+                wq::cp_async_commit();  // an empty group keeps the count uniform
+            wq::cp_async_wait<1>();
+            __syncwarp();
+            const unsigned char* sg = ring + st * kStageBytes;
+            // this lane's positions (chunk-relative): keys n = gr of both
+            // n-tiles; C fragment and value positions 2qc + {0, 1}, 8 + 2qc + {0, 1}
+            int pj[4];
+            pj[0] = 2 * qc;
+            pj[1] = 2 * qc + 1;
+            pj[2] = 8 + 2 * qc;
+            pj[3] = 9 + 2 * qc;
+            bool okj[4];
+            uint2 ksc[4], vsc[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const bool ok = rv[j] >= 0;
-                ksc[j] = ok ? __ldg(reinterpret_cast<const uint2*>(a.kd + rv[j] * (kD / 32))) : make_uint2(0u, 0u);
-                vsc[j] = ok ? __ldg(reinterpret_cast<const uint2*>(a.vd + rv[j] * (kD / 32))) : make_uint2(0u, 0u);
-#pragma unroll
-                for (int blk = 0; blk < 4; ++blk)
-                    vw[j][blk] = ok ? __ldg(reinterpret_cast<const uint32_t*>(a.vc + rv[j] * kD + 32 * blk + 4 * gr))
-                                    : 0u;
+                okj[j] = ((vm_cur >> pj[j]) & 1u) != 0;
+                ksc[j] = *reinterpret_cast<const uint2*>(sg + kOffKS + 8 * pj[j]);
+                vsc[j] = *reinterpret_cast<const uint2*>(sg + kOffVS + 8 * pj[j]);
             }
             // scores: sv[nt][i] = C fragment element i of n-tile nt (rows gr, gr, gr + 8, gr + 8;
             // positions base + 8 nt + 2 qc + {0, 1, 0, 1})
             float sv[2][4];
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
+                const int r = 8 * nt + gr;
 #pragma unroll
                 for (int e = 0; e < 4; ++e) sv[nt][e] = 0.f;
 #pragma unroll
                 for (int blk = 0; blk < 4; ++blk) {
+                    const uint2 kw = *reinterpret_cast<const uint2*>(
+                        sg + kOffK + r * kD + (swz(2 * blk + (qc >> 1), r) << 4) + ((qc & 1) << 3));
                     float acc[4] = {0.f, 0.f, 0.f, 0.f};
-                    const uint32_t u0 = kw[nt][blk].x ^ 0x80808080u, u1 = kw[nt][blk].y ^ 0x80808080u;
+                    const uint32_t u0 = kw.x ^ 0x80808080u, u1 = kw.y ^ 0x80808080u;
                     mma_f16(acc, qa[2 * blk], codes_f16x2(u0, 0x4140), codes_f16x2(u0, 0x4342));
                     mma_f16(acc, qa[2 * blk + 1], codes_f16x2(u1, 0x4140), codes_f16x2(u1, 0x4342));
                     const float d0 = scale_of(ksc[2 * nt], blk), d1 = scale_of(ksc[2 * nt + 1], blk);
@@ -434,10 +478,10 @@ __global__ void __launch_bounds__(kThreads) attn_split_tc_kernel(const AttnArgs 
                 }
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const int j = 2 * nt + (e & 1);                  // which of rv[]
+                    const int j = 2 * nt + (e & 1);                  // which of pj[]
                     const int t = base + 8 * nt + 2 * qc + (e & 1);  // its position
                     const int qp = e < 2 ? qp0 : qp1;
-                    sv[nt][e] = (rv[j] >= 0 && t <= qp) ? sv[nt][e] * ssc : -INFINITY;
+                    sv[nt][e] = (okj[j] && t <= qp) ? sv[nt][e] * ssc : -INFINITY;
                 }
             }
             // online softmax per row: maxima over the chunk's 16 positions (own
@@ -495,8 +539,8 @@ __global__ void __launch_bounds__(kThreads) attn_split_tc_kernel(const AttnArgs 
                 float ds[4];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) ds[j] = scale_of(vsc[j], blk) * evs;
-                // A: rows gr / gr + 8, k = 2qc, 2qc + 1 (positions rv[0], rv[1]) and
-                // k = 2qc + 8, 2qc + 9 (rv[2], rv[3])
+                // A: rows gr / gr + 8, k = 2qc, 2qc + 1 (positions pj[0], pj[1]) and
+                // k = 2qc + 8, 2qc + 9 (pj[2], pj[3])
                 uint32_t ah[4], al[4];
                 split_f16x2(p[0][0] * ds[0], p[0][1] * ds[1], ah[0], al[0]);
                 split_f16x2(p[0][2] * ds[0], p[0][3] * ds[1], ah[1], al[1]);
@@ -504,10 +548,15 @@ __global__ void __launch_bounds__(kThreads) attn_split_tc_kernel(const AttnArgs 
                 split_f16x2(p[1][2] * ds[2], p[1][3] * ds[3], ah[3], al[3]);
                 // B: the four positions' codes at dims 32 blk + 4 gr + j, transposed
                 // so that each 16-bit half holds two positions at one dim
-                const uint32_t u0 = vw[0][blk] ^ 0x80808080u, u1 = vw[1][blk] ^ 0x80808080u;
-                const uint32_t u2 = vw[2][blk] ^ 0x80808080u, u3 = vw[3][blk] ^ 0x80808080u;
-                const uint32_t t01a = __byte_perm(u0, u1, 0x5140), t01b = __byte_perm(u0, u1, 0x7362);
-                const uint32_t t23a = __byte_perm(u2, u3, 0x5140), t23b = __byte_perm(u2, u3, 0x7362);
+                uint32_t u[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    u[j] = *reinterpret_cast<const uint32_t*>(
+                               sg + kOffV + pj[j] * kD + (swz(2 * blk + (gr >> 2), pj[j]) << 4) +
+                               ((gr & 3) << 2)) ^
+                           0x80808080u;
+                const uint32_t t01a = __byte_perm(u[0], u[1], 0x5140), t01b = __byte_perm(u[0], u[1], 0x7362);
+                const uint32_t t23a = __byte_perm(u[2], u[3], 0x5140), t23b = __byte_perm(u[2], u[3], 0x7362);
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const uint32_t lo = j < 2 ? t01a : t01b, hi = j < 2 ? t23a : t23b;
@@ -517,7 +566,10 @@ __global__ void __launch_bounds__(kThreads) attn_split_tc_kernel(const AttnArgs 
                     mma_f16(o[4 * blk + j], al, b0, b1);
                 }
             }
+            __syncwarp();  // every lane has read stage st before it is refilled
+            vm_cur = vm_next;
         }
+        wq::cp_async_wait<0>();
         // this warp's state: maxima (uniform in the quad), sums over the quad,
         // O without its 2^ev
 #pragma unroll
@@ -532,6 +584,7 @@ __global__ void __launch_bounds__(kThreads) attn_split_tc_kernel(const AttnArgs 
             wl[warp][gr + 8] = l1;
         }
         const float inv = pow2i(-min(ev, 126));
+        __syncthreads();  // every warp is out of its copy ring before it becomes wacc
 #pragma unroll
         for (int blk = 0; blk < 4; ++blk)
 #pragma unroll
@@ -583,13 +636,13 @@ __global__ void __launch_bounds__(kD) attn_combine_kernel(const float* part, int
     out[vec * kD + d] = lt > 0.f ? at / lt : 0.f;
 }
 
-// Slices per sequence: about four CTAs per SM over the whole grid (two waves
-// at two resident CTAs per SM), no slice under 256 positions, at most 64; the
-// slice length rounded up to 128 positions (whole iterations of the CUDA-core
-// kernel's four warps of 32 positions).
-int splits_for(int max_seq_len, int B, int Hkv, int sms, int* chunk) {
+// Slices per sequence: one wave of CTAs over the grid (slots = SMs x the
+// tensor-core kernel's resident CTAs per SM), no slice under 256 positions,
+// at most 64; the slice length rounded up to 128 positions (whole iterations
+// of the CUDA-core kernel's four warps of 32 positions).
+int splits_for(int max_seq_len, int B, int Hkv, int slots, int* chunk) {
     const long long heads = static_cast<long long>(B) * Hkv;
-    long long want = 4LL * sms / (heads > 0 ? heads : 1);
+    long long want = slots / (heads > 0 ? heads : 1);
     const long long most = (static_cast<long long>(max_seq_len) + 255) / 256;
     if (want > most) want = most;
     if (want > 64) want = 64;
@@ -600,6 +653,19 @@ int splits_for(int max_seq_len, int B, int Hkv, int sms, int* chunk) {
     return static_cast<int>((max_seq_len + c - 1) / c);
 }
 
+// CTAs the device holds at once: SMs x resident tensor-core split CTAs per SM.
+wq_status_t grid_slots(int* slots) {
+    int sms = 0;
+    if (wq_status_t st = wq::host_sm_count(&sms)) return st;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attn_split_tc_kernel, kThreads, 0) !=
+            cudaSuccess ||
+        per_sm < 1)
+        per_sm = 1;
+    *slots = sms * per_sm;
+    return WQ_OK;
+}
+
 bool aligned(const void* p, size_t n) { return reinterpret_cast<uintptr_t>(p) % n == 0; }
 
 }  // namespace
@@ -608,10 +674,10 @@ extern "C" {
 
 size_t wq_paged_attention_workspace_bytes(int rows, int Hq, int Hkv, int B, int max_seq_len) {
     if (rows < 0 || Hq <= 0 || Hkv <= 0 || B <= 0 || max_seq_len <= 0) return 0;
-    int sms = 0;
-    if (wq::host_sm_count(&sms) != WQ_OK) return 0;
+    int slots = 0;
+    if (grid_slots(&slots) != WQ_OK) return 0;
     int chunk = 0;
-    const int splits = splits_for(max_seq_len, B, Hkv, sms, &chunk);
+    const int splits = splits_for(max_seq_len, B, Hkv, slots, &chunk);
     return wq::kWsHeader + static_cast<size_t>(rows) * Hq * splits * (2 + kD) * sizeof(float);
 }
 
@@ -658,9 +724,9 @@ wq_status_t paged_attention(const uint16_t* q, const int8_t* k_codes, const uint
     a.Hkv = Hkv;
     a.T = T;
     a.pages = pages;
-    int sms = 0;
-    if (wq_status_t st = wq::host_sm_count(&sms)) return st;
-    a.splits = splits_for(max_seq_len, B, Hkv, sms, &a.chunk);
+    int slots = 0;
+    if (wq_status_t st = grid_slots(&slots)) return st;
+    a.splits = splits_for(max_seq_len, B, Hkv, slots, &a.chunk);
     a.err = static_cast<int*>(workspace);
     a.part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + wq::kWsHeader);
     // every (row, head, slice) state is written: rows of other sequences are
