@@ -79,6 +79,10 @@ CASES = [
     synth.PagedAttention("a2", (5, 3, 300, 1024), 3, 40, 8, 128, 64, 22, shared_prefix=0),
     synth.PagedAttention("a3", (2048, 700), 1, 16, 16, 128, 32, 23, shared_prefix=512),
     synth.PagedAttention("a4", (4096, 33, 129, 3000), 3, 10, 2, 128, 64, 24, shared_prefix=0),
+    # more query vectors per key/value head than one pass holds: 4 rows x 5
+    # heads (passes of 15 and 5), and 7 rows x 16 heads (one row per pass)
+    synth.PagedAttention("a5", (300, 77, 1500), 4, 20, 4, 128, 32, 25, shared_prefix=64),
+    synth.PagedAttention("a6", (129, 40), 7, 16, 1, 128, 16, 26, shared_prefix=0),
 ]
 
 
