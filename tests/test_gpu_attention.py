@@ -136,18 +136,27 @@ def test_attention_is_deterministic_and_placement_free():
     assert (a.view(np.uint32) == c.view(np.uint32)).all()
 
 
-def test_bad_page_is_reported():
+@pytest.mark.parametrize("fault", ["page-outside-pool", "position-past-sequence"])
+def test_bad_table_is_reported(fault):
+    # the kernels check every table entry and position before reading: the
+    # error word says 2 and the affected rows read nothing
     import weight_only_bit_wq_gb300 as wq
     p = CASES[0]
-    d = synth.gen_paged_attention(p)
-    d = dict(d)
-    d["page_table"] = d["page_table"].copy()
-    d["page_table"][1, 2] = d["kc"].shape[0] + 5  # outside the pool
+    d = dict(synth.gen_paged_attention(p))
+    if fault == "page-outside-pool":
+        d["page_table"] = d["page_table"].copy()
+        d["page_table"][1, 2] = d["kc"].shape[0] + 5
+    else:
+        d["row_pos"] = d["row_pos"].copy()
+        d["row_pos"][0] = int(d["seq_len"][d["row_seq"][0]]) + 3
     n = int(wq._lib().wq_paged_attention_workspace_bytes(len(d["row_seq"]), p.Hq, p.Hkv,
                                                           len(p.seq_lens), int(d["seq_len"].max())))
     ws = torch.zeros(n, dtype=torch.uint8, device=dev())
-    _run(d, workspace=ws)
+    got = _run(d, workspace=ws)
     assert int(ws[:4].view(torch.int32).item()) == 2
+    assert np.isfinite(got).all()
+    if fault == "position-past-sequence":
+        assert (got[0] == 0).all()
 
 
 # The workload the benchmark times: four agents x 32768 positions of their own
