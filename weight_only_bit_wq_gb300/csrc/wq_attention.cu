@@ -238,7 +238,7 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnArgs a) 
 //           about 22 significant bits); O carries 2^ev until the end.
 // The head dims are assigned to k (and, for the values, to n) in a permuted
 // order so that each lane's codes come from one 8-byte (keys) or 4-byte
-// (values) load: for k-step 2 * blk + hh, lane quad position c holds k =
+// (values) shared-memory read: for k-step 2 * blk + hh, lane quad position c holds k =
 // 2c, 2c + 1 as dims 32 blk + 8c + 4hh + {0, 1} and k = 2c + 8, 2c + 9 as
 // dims 32 blk + 8c + 4hh + {2, 3}, the same for the query vectors (A) and the
 // keys (B); value n-tile 4 blk + j holds n = lane group r as dim 32 blk + 4r + j.
