@@ -525,12 +525,16 @@ __global__ void __launch_bounds__(kThreads) attn_split_tc_kernel(const AttnArgs 
                 r1 *= f;
                 ev = ev_c;
             }
+            // once the running maxima settle, most chunks leave O as it is
+            // (multiplying by 1 would change nothing)
+            if (__any_sync(0xffffffffu, r0 != 1.f || r1 != 1.f)) {
 #pragma unroll
-            for (int n = 0; n < 16; ++n) {
-                o[n][0] *= r0;
-                o[n][1] *= r0;
-                o[n][2] *= r1;
-                o[n][3] *= r1;
+                for (int n = 0; n < 16; ++n) {
+                    o[n][0] *= r0;
+                    o[n][1] *= r0;
+                    o[n][2] *= r1;
+                    o[n][3] *= r1;
+                }
             }
             const float evs = pow2i(min(ev, 127));
             // values, one 32-dim block at a time
