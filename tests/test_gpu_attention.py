@@ -83,6 +83,10 @@ CASES = [
     # heads (passes of 15 and 5), and 7 rows x 16 heads (one row per pass)
     synth.PagedAttention("a5", (300, 77, 1500), 4, 20, 4, 128, 32, 25, shared_prefix=64),
     synth.PagedAttention("a6", (129, 40), 7, 16, 1, 128, 16, 26, shared_prefix=0),
+    # 17-token pages (positions straddle pages at every offset), a one-token
+    # sequence, and a shared 17-token prefix
+    synth.PagedAttention("a7", (50, 1, 17, 260), 1, 6, 3, 128, 17, 27, shared_prefix=0),
+    synth.PagedAttention("a8", (34, 51, 90), 2, 6, 3, 128, 17, 28, shared_prefix=17),
 ]
 
 
