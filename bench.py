@@ -52,6 +52,7 @@ def parse_args(argv=None):
     ap.add_argument("--m", type=int, default=HEADLINE_M, help="headline stacked-row count")
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-configs", action="store_true")
+    ap.add_argument("--no-attention", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU oracle sample budget")
     ap.add_argument("--layers", type=int, default=64)
     ap.add_argument("--profile-config", default=None,
@@ -458,6 +459,74 @@ def run_configs(device, stream, peak, l2_bytes):
     return out
 
 
+# Decode attention over the paged q8_0 pool: four agents, each with 32768
+# positions of its own sequence (a 4096-token system prompt stored once and
+# shared), three query rows per agent (one token, two drafts), 40 query heads
+# over 8 key/value heads of 128 dims, 64-token pages: 118,784 tokens in the pool.
+ATTN_CASE = dict(seq_lens=(32768,) * 4, rows_per_seq=3, Hq=40, Hkv=8, D=128, T=64, seed=31,
+                 shared_prefix=4096)
+
+
+def attention_bytes(p):
+    """Algorithmic bytes of one call: every sequence reads its positions' K and V
+    codes and scales once (the shared prefix once per sequence), plus q and out."""
+    kv = sum(p.seq_lens) * p.Hkv * 2 * (p.D + 2 * (p.D // 32))
+    rows = len(p.seq_lens) * p.rows_per_seq
+    return kv + rows * p.Hq * p.D * (2 + 4)
+
+
+def run_attention(device, stream, peak, steps, warmup):
+    """µs per call of wq_paged_attention (tensor-core kernel) and, for context,
+    of the CUDA-core kernel, on the pool above (every call reads more than L2)."""
+    import ctypes
+
+    import torch
+
+    import synth
+    import weight_only_bit_wq_gb300 as wq
+
+    p = synth.PagedAttention("bench", **ATTN_CASE)
+    t = synth.gen_paged_attention_torch(p, device)
+    rows, Hq, D = t["q"].shape
+    pages, Hkv, T, _ = t["kc"].shape
+    B, max_pages = t["page_table"].shape
+    msl = max(p.seq_lens)
+    out = torch.empty((rows, Hq, D), dtype=torch.float32, device=device)
+    n = int(wq._lib().wq_paged_attention_workspace_bytes(rows, Hq, Hkv, B, msl))
+    ws = torch.zeros(max(n, 256), dtype=torch.uint8, device=device)
+    lib = wq._lib()
+    cc = lib.wq_internal_paged_attention_cuda_cores
+    cc.argtypes = lib.wq_paged_attention.argtypes
+    cc.restype = ctypes.c_int
+    ptr = lambda x: ctypes.c_void_p(x.data_ptr())
+    args = (ptr(t["q"]), ptr(t["kc"]), ptr(t["kd"]), ptr(t["vc"]), ptr(t["vd"]),
+            ptr(t["page_table"]), max_pages, ptr(t["seq_len"]), B, ptr(t["row_seq"]),
+            ptr(t["row_pos"]), rows, msl, Hq, Hkv, D, T, pages, ptr(out), ptr(ws), ws.numel(),
+            ctypes.c_void_p(stream.cuda_stream))
+    stream.wait_stream(torch.cuda.current_stream())
+    nbytes = attention_bytes(p)
+    res = {"workload": "decode attention over a paged q8_0 pool: 4 sequences x 32768 positions "
+                       "(4096-token prefix stored once), 3 query rows each, 40 query / 8 kv heads "
+                       "of 128, 64-token pages", "bytes_per_call": nbytes}
+    for name, fn in (("tensor_cores", lib.wq_paged_attention), ("cuda_cores", cc)):
+        def launch():
+            st = fn(*args)
+            if st != 0:
+                raise RuntimeError(f"{name}: status {st}")
+        ms = time_launches(launch, stream, steps, warmup, None)
+        us = ms * 1e3
+        res[name] = {"us_per_call": round(us, 2),
+                     "achieved_gbs": round(nbytes / (us * 1e-6) / 1e9, 1),
+                     "frac": round(nbytes / (us * 1e-6) / 1e9 / peak, 4)}
+    torch.cuda.synchronize()
+    word = int(ws[:4].view(torch.int32).item())
+    if word != 0:
+        raise RuntimeError(f"attention error word {word}")
+    del t, out, ws
+    torch.cuda.empty_cache()
+    return res
+
+
 # ------------------------------------------------------------ CPU oracle
 def cpu_sample(M, row_budget):
     """A bounded sample of the decode step: the first rows of layer 0's gate/up and down."""
@@ -665,6 +734,9 @@ def main_ours(args):
     configs = None
     if rank == 0 and not args.no_configs:
         configs = run_configs(device, stream, peak, l2)
+    attention = None
+    if rank == 0 and not args.no_attention:
+        attention = run_attention(device, stream, peak, max(3, args.steps // 2), 3)
     barrier(dist)
     cpu = cpu_baseline(args.m, args.cpu_seconds) if (rank == 0 and world == 1) else None
     clock_info = clocks.summary() if clocks is not None else None
@@ -685,7 +757,7 @@ def main_ours(args):
                          "launch_us": round(ms_max * 1e3 / n_launch, 3),
                          "timing": timing,
                          "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)"},
-            "step_modes": modes, "single_launch": single,
+            "step_modes": modes, "single_launch": single, "attention": attention,
             "cpu_baseline": cpu,
             "e2e": {"value": round(packed_all / (e2e_max * 1e-3) / 1e9, 1), "unit": "GB/s",
                     "h2d_bytes_per_step": head["h2d_bytes"], "d2h_bytes_per_step": head["d2h_bytes"],

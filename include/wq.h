@@ -279,6 +279,38 @@ wq_status_t wq_step_graph_create_ex(const wq_proj_desc_t* projs, int count, unsi
 wq_status_t wq_step_graph_launch(wq_step_graph_t graph, void* stream);
 void wq_step_graph_destroy(wq_step_graph_t graph);
 
+/*
+ * wq_paged_attention — decode attention over a paged q8_0 KV pool (OpenJet
+ * news page, paragraphs after "并行解码的原理": one shared pool in q8_0,
+ * managed in pages; attention, each agent reading its own cache, is what grows
+ * with the agents).  Query row i attends to positions 0 .. row_pos[i] of
+ * sequence row_seq[i]; query head h reads key/value head h / (Hq / Hkv):
+ *   out[i][h] = sum_t softmax_t(q[i][h] . k[t] / sqrt(D)) v[t]
+ * with k and v dequantised from q8_0 (blocks of 32 signed 8-bit codes along
+ * the head dimension, value = binary16 scale * code).
+ *
+ * Layout (device pointers): q bf16 [rows][Hq][D]; k_codes, v_codes int8
+ * [pages][Hkv][T][D] (16-byte aligned); k_scales, v_scales binary16
+ * [pages][Hkv][T][D/32] (8-byte aligned); page_table int32 [B][max_pages] (sequence b's token t
+ * in physical page page_table[b][t / T], slot t % T; pages may be shared);
+ * seq_len int32 [B]; row_seq, row_pos int32 [rows]; out fp32 [rows][Hq][D].
+ * D = 128; Hq a multiple of Hkv with Hq / Hkv <= 16; max_seq_len (host) bounds
+ * every seq_len and max_pages * T >= max_seq_len.  workspace: at least
+ * wq_paged_attention_workspace_bytes(rows, Hq, Hkv, B, max_seq_len) bytes (the
+ * slices per sequence follow the current device's size), 16-byte
+ * aligned, its first word zero; a page index outside the pool, a position
+ * past its sequence or a sequence longer than max_seq_len sets that word to 2
+ * (the affected rows read nothing).  Rows whose row_seq is not in [0, B)
+ * produce zeros.  Deterministic: the same inputs give the same bits.
+ */
+size_t wq_paged_attention_workspace_bytes(int rows, int Hq, int Hkv, int B, int max_seq_len);
+wq_status_t wq_paged_attention(const uint16_t* q, const int8_t* k_codes, const uint16_t* k_scales,
+                               const int8_t* v_codes, const uint16_t* v_scales,
+                               const int* page_table, int max_pages, const int* seq_len, int B,
+                               const int* row_seq, const int* row_pos, int rows, int max_seq_len,
+                               int Hq, int Hkv, int D, int T, int pages, float* out,
+                               void* workspace, size_t workspace_bytes, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -302,6 +302,56 @@ def gen_paged_attention(p: PagedAttention) -> Dict[str, np.ndarray]:
     pool, bf16 N(0,1) queries, and page tables that place each sequence's
     logical pages on distinct physical pages in a seeded shuffled order (the
     shared prefix's pages are the same physical pages in every sequence)."""
+    out, shape = _paged_tables(p)
+    n_codes = int(np.prod(shape))
+    n_scales = n_codes // 32
+    for i, kv in enumerate(("k", "v")):
+        cu = draws_u64(stream_key(p.seed, "kv_code", i), np.arange(n_codes, dtype=np.uint64))
+        out[kv + "c"] = (_uniform_int(cu, 0, 254) - 127).astype(np.int8).reshape(shape)
+        su = draws_u64(stream_key(p.seed, "kv_scale", i), np.arange(n_scales, dtype=np.uint64))
+        d32 = _uniform_f32(su, *p.scale_range)
+        out[kv + "d"] = d32.astype(np.float16).view(np.uint16).reshape(shape[:3] + (p.D // 32,))
+    return out
+
+
+def gen_paged_attention_torch(p: PagedAttention, device, chunk: int = 1 << 22):
+    """The values of ``gen_paged_attention``, with the K and V codes and scales
+    built on ``device`` by torch int64/float32 ops (the page tables and queries
+    are small and come from the host).  Codes are int8 tensors, scales and
+    queries int16 tensors holding the binary16 / bf16 bit patterns, the
+    tables int32 tensors."""
+    import torch
+
+    host, shape = _paged_tables(p)
+    out = {"q": torch.from_numpy(host["q"].view(np.int16)).to(device)}
+    for k in ("page_table", "seq_len", "row_seq", "row_pos"):
+        out[k] = torch.from_numpy(np.ascontiguousarray(host[k], dtype=np.int32)).to(device)
+    n_codes = int(np.prod(shape))
+    n_scales = n_codes // 32
+    a32 = torch.tensor(np.float32(p.scale_range[0]), device=device)
+    b32 = torch.tensor(np.float32(p.scale_range[1]), device=device)
+    for i, kv in enumerate(("k", "v")):
+        codes = torch.empty(n_codes, dtype=torch.int8, device=device)
+        key = stream_key(p.seed, "kv_code", i)
+        for c0 in range(0, n_codes, chunk):
+            c1 = min(n_codes, c0 + chunk)
+            u = _t_draws(key, torch.arange(c0, c1, dtype=torch.int64, device=device))
+            codes[c0:c1] = ((_t_lshr(u, 32) * 255) >> 32).sub_(127).to(torch.int8)
+        out[kv + "c"] = codes.view(shape)
+        scales = torch.empty(n_scales, dtype=torch.int16, device=device)
+        key = stream_key(p.seed, "kv_scale", i)
+        for c0 in range(0, n_scales, chunk):
+            c1 = min(n_scales, c0 + chunk)
+            u24 = _t_lshr(_t_draws(key, torch.arange(c0, c1, dtype=torch.int64, device=device)),
+                          40).to(torch.float32) * (2.0 ** -24)
+            scales[c0:c1] = (a32 + (b32 - a32) * u24).to(torch.float16).view(torch.int16)
+        out[kv + "d"] = scales.view(shape[:3] + (p.D // 32,))
+    return out
+
+
+def _paged_tables(p: PagedAttention):
+    """Page tables, sequence lengths, query rows and bf16 queries of ``p``,
+    and the shape [pages][Hkv][T][D] of the pool's code arrays."""
     B = len(p.seq_lens)
     assert p.shared_prefix % p.T == 0 and all(n >= p.shared_prefix for n in p.seq_lens)
     assert all(n >= p.rows_per_seq for n in p.seq_lens)
@@ -318,15 +368,7 @@ def gen_paged_attention(p: PagedAttention) -> Dict[str, np.ndarray]:
         table[b, n_shared:n_shared + own[b]] = order[nxt:nxt + own[b]]
         nxt += own[b]
     shape = (pages, p.Hkv, p.T, p.D)
-    n_codes = int(np.prod(shape))
-    n_scales = n_codes // 32
     out = {}
-    for i, kv in enumerate(("k", "v")):
-        cu = draws_u64(stream_key(p.seed, "kv_code", i), np.arange(n_codes, dtype=np.uint64))
-        out[kv + "c"] = (_uniform_int(cu, 0, 254) - 127).astype(np.int8).reshape(shape)
-        su = draws_u64(stream_key(p.seed, "kv_scale", i), np.arange(n_scales, dtype=np.uint64))
-        d32 = _uniform_f32(su, *p.scale_range)
-        out[kv + "d"] = d32.astype(np.float16).view(np.uint16).reshape(shape[:3] + (p.D // 32,))
     rows = B * p.rows_per_seq
     qn = _normal_f32(stream_key(p.seed, "attn_q"), np.arange(rows * p.Hq * p.D, dtype=np.uint64))
     out["q"] = f32_to_bf16_bits(qn).reshape(rows, p.Hq, p.D)
@@ -335,4 +377,4 @@ def gen_paged_attention(p: PagedAttention) -> Dict[str, np.ndarray]:
     out["row_seq"] = np.repeat(np.arange(B, dtype=np.int32), p.rows_per_seq)
     out["row_pos"] = np.concatenate([np.arange(n - p.rows_per_seq, n, dtype=np.int32)
                                      for n in p.seq_lens])
-    return out
+    return out, shape

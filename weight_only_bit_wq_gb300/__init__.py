@@ -27,7 +27,8 @@ EXPORTED = ("wq_abi_version", "wq_status_string", "wq_last_cuda_error", "wq_pack
             "wq_gemm", "wq_gemm_swiglu", "wq_check_workspace", "wq_gemm_noalloc", "wq_check_noalloc",
             "wq_step_workspace_bytes", "wq_step_run",
             "wq_step_run_ex", "wq_step_graph_create", "wq_step_graph_create_ex",
-            "wq_step_graph_launch", "wq_step_graph_destroy")
+            "wq_step_graph_launch", "wq_step_graph_destroy", "wq_paged_attention_workspace_bytes",
+            "wq_paged_attention")
 
 # Step modes (include/wq.h).
 WQ_STEP_FUSED = 1
@@ -77,6 +78,8 @@ def _lib() -> ctypes.CDLL:
             "wq_check_workspace": ([P, P], I),
             "wq_gemm_noalloc": ([P, P, P, P, P, I, I, I, I, I, P], I),
             "wq_check_noalloc": ([P], I),
+            "wq_paged_attention_workspace_bytes": ([I, I, I, I, I], S),
+            "wq_paged_attention": ([P, P, P, P, P, P, I, P, I, P, P, I, I, I, I, I, I, I, P, P, S, P], I),
             "wq_step_workspace_bytes": ([P, I, ctypes.c_uint], S),
             "wq_step_run": ([P, I, P, S, P], I),
             "wq_step_run_ex": ([P, I, ctypes.c_uint, P, S, P], I),
@@ -191,6 +194,31 @@ def wq_gemm_swiglu(x, wq, scales, zeros, N: int, group: int, bits: int, out=None
     _check(_lib().wq_gemm_swiglu(_ptr(x), _ptr(wq), _ptr(scales), _ptr(zeros), _ptr(out), M, N, K,
                                  group, bits, _ptr(workspace), nbytes, _stream(stream)),
            "wq_gemm_swiglu")
+    return out
+
+
+def wq_paged_attention(q, kc, kd, vc, vd, page_table, seq_len, row_seq, row_pos, max_seq_len: int,
+                       out=None, workspace=None, stream=None) -> torch.Tensor:
+    """fp32 [rows][Hq][D] decode attention over a paged q8_0 pool (include/wq.h).
+
+    q bf16 [rows][Hq][D]; kc, vc int8 [pages][Hkv][T][D]; kd, vd binary16 bits
+    [pages][Hkv][T][D/32]; page_table int32 [B][max_pages]; seq_len int32 [B];
+    row_seq, row_pos int32 [rows]; all on the device.  The workspace's first word
+    is the kernel's error word (2: a table entry outside the pool)."""
+    rows, Hq, D = q.shape
+    pages, Hkv, T, _ = kc.shape
+    B, max_pages = page_table.shape
+    if out is None:
+        out = torch.empty((rows, Hq, D), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        n = int(_lib().wq_paged_attention_workspace_bytes(rows, Hq, Hkv, B, max_seq_len))
+        workspace = torch.zeros(max(n, 256), dtype=torch.uint8, device=q.device)
+    nbytes = workspace.numel() * workspace.element_size()
+    _check(_lib().wq_paged_attention(_ptr(q), _ptr(kc), _ptr(kd), _ptr(vc), _ptr(vd),
+                                     _ptr(page_table), max_pages, _ptr(seq_len), B, _ptr(row_seq),
+                                     _ptr(row_pos), rows, max_seq_len, Hq, Hkv, D, T, pages,
+                                     _ptr(out), _ptr(workspace), nbytes, _stream(stream)),
+           "wq_paged_attention")
     return out
 
 
