@@ -7,8 +7,9 @@ This file is collected last on purpose.  Its checks, through the C ABI: two
 calls in a row give Y bit for bit equal to wq_gemm's (the same kernel with the
 same split; the second call sees whatever the first left in the shared array)
 and within the GEMM tolerance of the fp64 oracle; the array's error word reads
-back clean (wq_check_noalloc); and a problem too large for the fixed array is
-refused up front.
+back clean (wq_check_noalloc); a 300,160-row problem runs; a problem whose
+counters would not fit the fixed array, and bad arguments, are refused before
+anything is launched.
 """
 import ctypes
 
@@ -67,11 +68,33 @@ def test_noalloc_matches_wq_gemm_and_oracle_twice(lib):
         assert lib.wq_check_noalloc(_stream()) == wq.WQ_OK
 
 
-def test_noalloc_refuses_oversized_problem(lib):
+def test_noalloc_tall_problem_runs_oversized_is_refused(lib):
+    # The fixed array holds the split-K partials (two slots per CTA) and 64
+    # bytes of arrival counters per 128-row tile: a 300,160-row problem fits and
+    # matches wq_gemm bit for bit; 2^30 rows (2^23 tiles, 512 MiB of counters)
+    # do not and are refused before anything is launched, as are bad arguments.
     import weight_only_bit_wq_gb300 as wq
-    P = ctypes.c_void_p
-    # 2^30 rows = 2^23 tiles x 64 bytes of arrival counters = 512 MiB: far beyond
-    # the fixed 8 MiB array; refused before anything is launched
-    st = lib.wq_gemm_noalloc(P(16), P(16), P(16), P(16), P(16), 1, 1 << 30, 128, 128, 4, _stream())
-    assert st == wq.WQ_ERR_INVALID_ARG
+    p = synth.Projection("tall", 3, 300160, 256, 4, 128, 903)
+    q, s, z = synth.gen_weights_torch(p, dev())
+    wqw = wq.wq_pack(q, p.bits)
+    x = torch.from_numpy(synth.gen_x(p).view(np.int16)).to(dev())
+    ref = wq.wq_gemm(x, wqw, s, z, p.N, p.group, p.bits).cpu().numpy()
+    y = torch.full((p.M, p.N), float("nan"), dtype=torch.float32, device=dev())
+    st = lib.wq_gemm_noalloc(ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(wqw.data_ptr()),
+                             ctypes.c_void_p(s.data_ptr()), ctypes.c_void_p(z.data_ptr()),
+                             ctypes.c_void_p(y.data_ptr()), p.M, p.N, p.K, p.group, p.bits,
+                             _stream())
+    assert st == wq.WQ_OK
+    assert np.array_equal(y.cpu().numpy().view(np.uint32), ref.view(np.uint32))
     assert lib.wq_check_noalloc(_stream()) == wq.WQ_OK
+    P = ctypes.c_void_p
+    # refused on the host: the pointers below are never touched
+    assert lib.wq_gemm_noalloc(P(16), P(16), P(16), P(16), P(16), 1, 1 << 30, 128, 128, 4,
+                               _stream()) == wq.WQ_ERR_INVALID_ARG
+    # M > 32, an odd group size and K not a multiple of the group
+    assert lib.wq_gemm_noalloc(P(16), P(16), P(16), P(16), P(16), 33, 128, 128, 128, 4,
+                               _stream()) == wq.WQ_ERR_INVALID_ARG
+    assert lib.wq_gemm_noalloc(P(16), P(16), P(16), P(16), P(16), 1, 128, 128, 96, 4,
+                               _stream()) == wq.WQ_ERR_INVALID_ARG
+    assert lib.wq_gemm_noalloc(P(16), P(16), P(16), P(16), P(16), 1, 128, 100, 32, 4,
+                               _stream()) == wq.WQ_ERR_INVALID_ARG

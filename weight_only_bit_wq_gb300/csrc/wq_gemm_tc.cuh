@@ -659,8 +659,9 @@ __device__ __forceinline__ void finish_rows(const Ctx& c, const ProjView& v,
                                             bool likely_last, int r, int q, int lane) {
     const int n = t * kBN + r;
     const int gt = v.toff + t;
+    // only phases that a later phase of the launch waits for are counted
     auto count_done = [&]() {
-        if (c.proj != nullptr) {
+        if (c.done != nullptr && v.phase + 1 < c.nphase) {
             __syncwarp();
             if (lane == 0) red_add_release_gpu(c.done + v.phase, 1);
         }
