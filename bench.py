@@ -56,7 +56,7 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU oracle sample budget")
     ap.add_argument("--layers", type=int, default=64)
     ap.add_argument("--profile-config", default=None,
-                    help="only run CALLS single wq_gemm calls of this config (for ncu captures)")
+                    help="only run CALLS calls of this config (a seeded GEMM config, \"step\" or \"attention\"; for ncu captures)")
     ap.add_argument("--calls", type=int, default=3)
     return ap.parse_args(argv)
 
@@ -821,6 +821,18 @@ def main_profile(args):
 
     __graft_entry__.build()
     device = torch.device("cuda", 0)
+    if args.profile_config == "attention":
+        pa = synth.PagedAttention("bench", **ATTN_CASE)
+        t = synth.gen_paged_attention_torch(pa, device)
+        for _ in range(args.calls):
+            out = wq.wq_paged_attention(t["q"], t["kc"], t["kd"], t["vc"], t["vd"],
+                                        t["page_table"], t["seq_len"], t["row_seq"], t["row_pos"],
+                                        max(pa.seq_lens))
+        torch.cuda.synchronize()
+        print(json.dumps({"profile_config": "attention", "calls": args.calls,
+                          "bytes_per_call": attention_bytes(pa),
+                          "max_abs_out": float(out.abs().max())}))
+        return 0
     if args.profile_config == "step":
         stack = StepStack(args.layers, device)
         _, _, _, descs = stack.buffers(args.m)

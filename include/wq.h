@@ -89,7 +89,8 @@ long wq_packed_words_per_row(int K, int bits);
  */
 wq_status_t wq_pack(const uint8_t* q, uint32_t* wq, int N, int K, int bits, void* stream);
 
-/* wq_unpack — inverse of wq_pack (a test aid): wq[N][W] -> q[N][K]. */
+/* wq_unpack — inverse of wq_pack (a test aid): wq[N][W] -> q[N][K].  No
+ * passage of the pages defines it; it exists to check the packed layout. */
 wq_status_t wq_unpack(const uint32_t* wq, uint8_t* q, int N, int K, int bits, void* stream);
 
 /*
@@ -103,9 +104,11 @@ wq_status_t wq_dequant(const uint32_t* wq, const uint16_t* scales, const uint8_t
                        uint16_t* w, int N, int K, int group, int bits, void* stream);
 
 /*
- * Workspace for wq_gemm on the CURRENT device: split-K partial sums and
- * per-tile arrival counters (it depends on N, K, bits and the SM count, never
- * on M).  Returns 0 for bad arguments.
+ * Workspace for wq_gemm on the CURRENT device (its SM count sets the grid):
+ * split-K partial sums and per-tile arrival counters (it depends on N and the
+ * SM count, never on M; call it with the device that will run the GEMM
+ * current).  Returns 0 for bad arguments.  No passage of the pages defines it;
+ * it sizes the library's own scratch.
  */
 size_t wq_workspace_bytes(int M, int N, int K, int group, int bits);
 
