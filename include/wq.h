@@ -252,6 +252,15 @@ typedef struct wq_proj_desc {
  *   results agree with wq_gemm to rounding, not bit for bit; a row alone is
  *   still bit-identical to the same row stacked. */
 #define WQ_STEP_FUSED 1u
+/* With WQ_STEP_FUSED: each dependency phase of a run (a projection whose
+ * `after` names a projection of the current phase starts a new one) is its own
+ * persistent launch over all of that phase's projections, and stream order --
+ * every launch after the first a programmatic dependent of the one before --
+ * replaces the device-side waits between phases.  Independent projections of a
+ * phase still share one launch and one stream-K split.  Results as
+ * WQ_STEP_FUSED (the split of each phase is the same).  Not part of the pages:
+ * a launch plan for the same step. */
+#define WQ_STEP_PHASES 2u
 
 /* Workspace bytes for a step in the given mode (0 for invalid input).  In
  * fused mode it holds the error word, split-K partials and counters, the

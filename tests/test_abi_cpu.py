@@ -136,6 +136,11 @@ def test_step_rejects_bad_flags_and_epilogues(wq):
     P = ctypes.c_void_p
     d, n = _descs(wq, [-1, 0])
     assert lib.wq_step_run_ex(d, n, 0x10, P(16), 1 << 20, P(0)) == wq.WQ_ERR_INVALID_ARG
+    # per-phase launches only exist as a variant of the fused mode
+    assert lib.wq_step_run_ex(d, n, wq.WQ_STEP_PHASES, P(16), 1 << 20, P(0)) == wq.WQ_ERR_INVALID_ARG
+    g = P(0)
+    assert lib.wq_step_graph_create_ex(d, n, wq.WQ_STEP_PHASES, P(16), 1 << 20, P(0),
+                                       ctypes.byref(g)) == wq.WQ_ERR_INVALID_ARG
     d, n = _descs(wq, [-1], epilogue=7)
     assert lib.wq_step_run_ex(d, n, 0, P(16), 1 << 20, P(0)) == wq.WQ_ERR_INVALID_ARG
     d, n = _descs(wq, [-1], epilogue=wq.WQ_EPI_SWIGLU, N=255)  # odd gate/up width

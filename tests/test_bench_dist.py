@@ -69,6 +69,10 @@ def test_headline_mode_is_the_faster_chain_mode():
     assert bench.choose_head({"fused": 5.17, "sequential": 4.96}) == "sequential"
     assert bench.choose_head({"fused": 4.0, "sequential": 4.96}) == "fused"
     assert bench.choose_head({"fused": 5.0, "sequential": 5.0}) == "fused"
+    assert bench.choose_head({"fused": 5.1, "phased": 4.2, "sequential": 4.9}) == "phased"
+    # launches per step with one launch per dependency phase: q, k, v share one
+    descs = [{"after": a} for a in bench.layer_dependencies(12)]
+    assert bench.count_phases(descs) == 8
     cfg = bench._config(16, 64, 1, "sequential", 384)
     assert cfg["launches_per_step"] == 384 and "sequential" in cfg["headline"]
     assert bench._config(16, 64, 1)["launches_per_step"] == 1

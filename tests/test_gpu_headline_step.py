@@ -12,7 +12,8 @@ build).  Rows are bitwise equal across the three row counts (batch
 invariance: OpenJet news page, "新提示不会让所有人停摆").  The sequential mode
 (one launch per projection) is checked against the oracle on the same rows; it
 splits each tile's K range differently from the fused launch, so the two agree
-to rounding, not bit for bit.
+to rounding, not bit for bit.  One launch per dependency phase gives the fused
+launch's results bit for bit.
 """
 import numpy as np
 import pytest
@@ -114,7 +115,12 @@ def test_fused_layer_chain_full_size_all_projections(stack):
         assert np.array_equal(a24[:16].view(np.uint32), a16.view(np.uint32)), i
 
 
-def test_sequential_full_size_all_projections(stack):
+def test_sequential_and_phased_full_size_all_projections(stack):
     import weight_only_bit_wq_gb300 as wq
     ys = _run(wq, stack, 16, 0)
     _check_oracle(stack, ys, 16, "sequential")
+    # one launch per dependency phase: the fused launch's split, bit for bit
+    fused = _run(wq, stack, 16, wq.WQ_STEP_FUSED)
+    phased = _run(wq, stack, 16, wq.WQ_STEP_FUSED | wq.WQ_STEP_PHASES)
+    for i, (a, b) in enumerate(zip(fused, phased)):
+        assert np.array_equal(a.view(np.uint32), b.view(np.uint32)), i

@@ -102,15 +102,24 @@ def test_fused_uniform_stack_matches_oracle(fmt, deps):
     after = _layer_after(len(projs)) if deps else None
     descs = _descs(wq, projs, after)
     ws = wq.new_step_workspace(descs, wq.WQ_STEP_FUSED)
-    for _ in range(2):  # the second run checks that counters were left clean
+    ref = None
+    # one launch for the run, then one launch per phase (the same split: bitwise equal)
+    for flags in (wq.WQ_STEP_FUSED, wq.WQ_STEP_FUSED, wq.WQ_STEP_FUSED | wq.WQ_STEP_PHASES,
+                  wq.WQ_STEP_FUSED | wq.WQ_STEP_PHASES):
         for p, w, x, d in projs:
             d["y"].fill_(float("nan"))
-        wq.wq_step_run(descs, ws, flags=wq.WQ_STEP_FUSED)
+        wq.wq_step_run(descs, ws, flags=flags)  # repeats check that counters were left clean
         torch.cuda.synchronize()
         wq.wq_check_workspace(ws)
-        for p, w, x, d in projs:
-            err = rel_err(d["y"].cpu().numpy(), oracle_gemm(p, w, x))
-            assert err <= REL_TOL and err <= ARITH_TOL, (p.name, err)
+        ys = [d["y"].cpu().numpy() for p, w, x, d in projs]
+        if ref is None:
+            ref = ys
+            for (p, w, x, d), y in zip(projs, ys):
+                err = rel_err(y, oracle_gemm(p, w, x))
+                assert err <= REL_TOL and err <= ARITH_TOL, (p.name, err)
+        else:
+            for (p, w, x, d), y, r in zip(projs, ys, ref):
+                assert np.array_equal(y.view(np.uint32), r.view(np.uint32)), (flags, p.name)
 
 
 @pytest.mark.parametrize("deps", [False, True], ids=["independent", "layer-chain"])

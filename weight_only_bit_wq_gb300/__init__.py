@@ -32,6 +32,7 @@ EXPORTED = ("wq_abi_version", "wq_status_string", "wq_last_cuda_error", "wq_pack
 
 # Step modes (include/wq.h).
 WQ_STEP_FUSED = 1
+WQ_STEP_PHASES = 2
 # Projection epilogues (include/wq.h).
 WQ_EPI_NONE, WQ_EPI_SWIGLU = 0, 1
 

@@ -486,6 +486,7 @@ struct Ctx {
     int* err;
     long long U;
     int P;
+    bool pdl;  // X and every write wait for the previous kernel on the stream
 
     __device__ __forceinline__ ProjView view(int p) const {
         if (proj == nullptr) return one;
@@ -1002,7 +1003,10 @@ __device__ __forceinline__ bool wait_deps(const Ctx& c, int upto, int& verified,
     }
 }
 
-template <int BITS, int G, int NC, bool MULTI, int EPI>
+// HOLD: the build can be launched as a programmatic dependent (single
+// projections always; a fused step only in its per-phase launches, a separate
+// build because the fused kernel's speed measured sensitive to any code added).
+template <int BITS, int G, int NC, bool MULTI, int EPI, bool HOLD = !MULTI>
 __global__ void __launch_bounds__(Lay<BITS, G, NC>::kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                    const GemmArgs a, const StepArgs sa) {
@@ -1028,6 +1032,7 @@ __global__ void __launch_bounds__(Lay<BITS, G, NC>::kThreads, 1)
         c.err = sa.err;
         c.U = sa.U;
         c.P = sa.P;
+        c.pdl = sa.pdl != 0;
     } else {
         c.proj = nullptr;
         c.phase = nullptr;
@@ -1056,6 +1061,7 @@ __global__ void __launch_bounds__(Lay<BITS, G, NC>::kThreads, 1)
         c.err = a.err;
         c.U = a.U;
         c.P = a.P;
+        c.pdl = a.pdl != 0;
     }
 
     // warp index through a shuffle so that the compiler treats it as uniform
@@ -1136,14 +1142,25 @@ __global__ void __launch_bounds__(Lay<BITS, G, NC>::kThreads, 1)
                 --q_n;
             }
         };
-        // A dependent launch (single projection) streams the packed words and
-        // zero points of its first stages at once; their X (and everything
-        // after) waits until the previous kernel has completed.  Two stages
-        // measured best: a longer hold releases a burst of X loads late.
+        // A dependent launch streams the packed words and zero points of its
+        // first stages at once; their X (and everything after) waits until the
+        // previous kernel has completed.  Two stages measured best: a longer
+        // hold releases a burst of X loads late.
         constexpr int kHeld = S < 2 ? S : 2;
-        const bool hold_x = !MULTI && a.pdl != 0;
+        const bool hold_x = HOLD && c.pdl;
         const int n_held = hold_x ? (n_units < kHeld ? n_units : kHeld) : 0;
-        const int u_first = static_cast<int>(c.sub_lo(0, blockIdx.x));
+        static_assert(kHeld <= 2, "held stages kept in two named slots");
+        const CUtensorMap* h_map0 = nullptr;
+        const CUtensorMap* h_map1 = nullptr;
+        int h_i0 = 0, h_i1 = 0;
+        bool h_x3d0 = false, h_x3d1 = false;
+        // X of the first `n` held stages (slots 0 and 1) once the previous
+        // kernel has completed
+        auto release_held = [&](int n) {
+            griddep_wait();
+            if (n > 0) issue_x(0u, h_map0, h_i0, h_x3d0);
+            if (n > 1) issue_x(1u, h_map1, h_i1, h_x3d1);
+        };
         Ring<S> st;
         uint32_t it = 0;
         bool ok = true;
@@ -1180,13 +1197,16 @@ __global__ void __launch_bounds__(Lay<BITS, G, NC>::kThreads, 1)
                         tma_load_2d(stage + b * L::kBoxBytes, cu.v.tmW,
                                     (cu.i * L::kBoxes + b) * kWordsPerStage, cu.t * kBN, fb, pol_w);
                     if (k < n_held) {
-                        if (k == n_held - 1) {
-                            // X of the held stages (slots 0.., units u_first..) once
-                            // the previous kernel has completed
-                            griddep_wait();
-                            for (int kk = 0; kk < n_held; ++kk)
-                                issue_x(static_cast<uint32_t>(kk), cu.v.tmX, (u_first + kk) % cu.v.I, cu.v.x3d);
+                        if (k == 0) {
+                            h_map0 = cu.v.tmX;
+                            h_i0 = cu.i;
+                            h_x3d0 = cu.v.x3d;
+                        } else {
+                            h_map1 = cu.v.tmX;
+                            h_i1 = cu.i;
+                            h_x3d1 = cu.v.x3d;
                         }
+                        if (k == n_held - 1) release_held(n_held);
                     } else if (!MULTI || cu.v.after < 0 || (q_n == 0 && deps_ready(c, cu.v.after, verified))) {
                         issue_x(st.slot, cu.v.tmX, cu.i, cu.v.x3d);
                     } else {
@@ -1264,11 +1284,7 @@ __global__ void __launch_bounds__(Lay<BITS, G, NC>::kThreads, 1)
             if (!ok) {
                 // stages whose X was still held back get it now (the previous
                 // kernel always completes), so that every stage in flight lands
-                if (hold_x && static_cast<int>(it) < n_held) {
-                    griddep_wait();
-                    for (int kk = 0; kk < static_cast<int>(it); ++kk)
-                        issue_x(static_cast<uint32_t>(kk), c.one.tmX, (u_first + kk) % c.one.I, c.one.x3d);
-                }
+                if (hold_x && static_cast<int>(it) < n_held) release_held(static_cast<int>(it));
                 // let copies already in flight land before the CTA's shared memory goes away
                 const uint32_t first = it > S ? it - S : 0;
                 volatile int never = 0;
@@ -1405,7 +1421,8 @@ cudaError_t launch_tc(const CUtensorMap& tmW, const CUtensorMap& tmX, const Gemm
 template <int BITS, int G, int NC>
 cudaError_t launch_step_nc(const StepArgs& sa, bool cooperative, cudaStream_t s) {
     using L = Lay<BITS, G, NC>;
-    auto kern = gemm_tc_kernel<BITS, G, NC, true, kEpiAny>;
+    auto kern = sa.pdl ? gemm_tc_kernel<BITS, G, NC, true, kEpiAny, true>
+                       : gemm_tc_kernel<BITS, G, NC, true, kEpiAny, false>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
     if (e != cudaSuccess) return e;
@@ -1417,8 +1434,13 @@ cudaError_t launch_step_nc(const StepArgs& sa, bool cooperative, cudaStream_t s)
     cfg.dynamicSmemBytes = L::kSmemBytes;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = cooperative ? 1 : 0;
+    if (sa.pdl) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+    } else {
+        attr[0].id = cudaLaunchAttributeCooperative;
+        attr[0].val.cooperative = cooperative ? 1 : 0;
+    }
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kern, none, none, a, sa);

@@ -90,6 +90,9 @@ struct StepArgs {
     int* err;
     long long U;          // total units
     int P;
+    int pdl;              // launched as a programmatic dependent of the previous kernel on the
+                          // stream (one phase, nothing waits): X is read, and anything written,
+                          // once that kernel completed
 };
 
 // Static stream-K schedule: CTA b owns units [unit_begin(b), unit_begin(b+1)).

@@ -158,6 +158,31 @@ wq_status_t build_table(const wq_proj_desc_t* projs, const Run& r, std::vector<w
     return WQ_OK;
 }
 
+// Per-phase launches (WQ_STEP_PHASES): phase p of a run becomes a launch of
+// its own over the projections [first[p], first[p + 1]) of the run, so its
+// table entries are rebased to the phase (units and tiles from 0, phase 0,
+// no dependency: stream order replaces the device-side waits) and phase p's
+// PhaseDev sits at the slot of its first projection.
+void to_phase_tables(std::vector<wq::ProjDev>& host, const std::vector<wq::PhaseDev>& phases,
+                     std::vector<wq::PhaseDev>& per_slot, std::vector<int>& first) {
+    const int n = static_cast<int>(host.size());
+    per_slot.assign(static_cast<size_t>(n), wq::PhaseDev{});
+    first.assign(phases.size() + 1, n);
+    for (int li = n - 1; li >= 0; --li) first[static_cast<size_t>(host[li].phase)] = li;
+    for (size_t p = 0; p < phases.size(); ++p) {
+        const int f = first[p];
+        per_slot[static_cast<size_t>(f)] = {0, phases[p].U, phases[p].need, 0};
+        const int toff0 = host[static_cast<size_t>(f)].toff;
+        for (int li = f; li < first[p + 1]; ++li) {
+            wq::ProjDev& d = host[static_cast<size_t>(li)];
+            d.uoff -= phases[p].uoff;
+            d.toff -= toff0;
+            d.phase = 0;
+            d.after = -1;
+        }
+    }
+}
+
 // Reset the run's completion counters and launch its persistent kernel.
 wq_status_t launch_run(const Run& r, Tables tab, int nphase, long long units, bool waits,
                        uint8_t* ws, const FusedLayout& lay, int sms, cudaStream_t s) {
@@ -165,7 +190,7 @@ wq_status_t launch_run(const Run& r, Tables tab, int nphase, long long units, bo
     int* done = reinterpret_cast<int*>(ws + lay.done_off);
     cudaError_t e = cudaMemsetAsync(done, 0, static_cast<size_t>(n) * sizeof(int), s);
     if (e != cudaSuccess) return wq::host_cuda_fail(e);
-    wq::StepArgs sa;
+    wq::StepArgs sa{};
     sa.proj = tab.proj + r.begin;
     sa.phase = tab.phase + r.begin;
     sa.nproj = n;
@@ -176,6 +201,7 @@ wq_status_t launch_run(const Run& r, Tables tab, int nphase, long long units, bo
     sa.err = reinterpret_cast<int*>(ws);
     sa.U = units;
     sa.P = static_cast<int>(std::min<long long>(sms, units));
+    sa.pdl = 0;
     if (r.bits == 4)
         e = wq::launch_step_b4(r.group, sa, waits, r.nc, s);
     else if (r.bits == 3)
@@ -183,6 +209,37 @@ wq_status_t launch_run(const Run& r, Tables tab, int nphase, long long units, bo
     else
         e = wq::launch_step_b2(r.group, sa, waits, r.nc, s);
     return e == cudaSuccess ? WQ_OK : wq::host_cuda_fail(e);
+}
+
+// One launch per phase of a run (tables from to_phase_tables); every launch
+// that follows another kernel of the step is a programmatic dependent one.
+wq_status_t launch_phases(const Run& r, Tables tab, const std::vector<wq::PhaseDev>& phases,
+                          const std::vector<int>& first, uint8_t* ws, const FusedLayout& lay,
+                          int sms, cudaStream_t s, bool& prev_kernel) {
+    for (size_t p = 0; p < phases.size(); ++p) {
+        wq::StepArgs sa{};
+        sa.proj = tab.proj + r.begin + first[p];
+        sa.phase = tab.phase + r.begin + first[p];
+        sa.nproj = first[p + 1] - first[p];
+        sa.nphase = 1;
+        sa.partials = reinterpret_cast<float*>(ws + lay.partial_off);
+        sa.counters = reinterpret_cast<int*>(ws + lay.counter_off);
+        sa.done = reinterpret_cast<int*>(ws + lay.done_off);
+        sa.err = reinterpret_cast<int*>(ws);
+        sa.U = phases[p].U;
+        sa.P = static_cast<int>(std::min<long long>(sms, phases[p].U));
+        sa.pdl = prev_kernel ? 1 : 0;
+        cudaError_t e;
+        if (r.bits == 4)
+            e = wq::launch_step_b4(r.group, sa, false, r.nc, s);
+        else if (r.bits == 3)
+            e = wq::launch_step_b3(r.group, sa, false, r.nc, s);
+        else
+            e = wq::launch_step_b2(r.group, sa, false, r.nc, s);
+        if (e != cudaSuccess) return wq::host_cuda_fail(e);
+        prev_kernel = true;
+    }
+    return WQ_OK;
 }
 
 wq_status_t run_single(const wq_proj_desc_t& p, void* workspace, size_t workspace_bytes,
@@ -210,19 +267,22 @@ wq_status_t run_sequential(const wq_proj_desc_t* projs, int count, void* workspa
 
 // Upload every run's tables to `base` (table_bytes(count) of device memory),
 // synchronously: graphs do this once before capturing.
-wq_status_t upload_tables(const wq_proj_desc_t* projs, int count, void* base) {
+wq_status_t upload_tables(const wq_proj_desc_t* projs, int count, void* base, bool phased) {
     const Tables tab = tables_at(base, count);
     std::vector<wq::ProjDev> host;
-    std::vector<wq::PhaseDev> phases;
+    std::vector<wq::PhaseDev> phases, per_slot;
+    std::vector<int> first;
     for (const Run& r : split_runs(projs, count)) {
         if (!r.fused) continue;
         long long units = 0;
         bool waits = false;
         if (wq_status_t st = build_table(projs, r, host, phases, &units, &waits)) return st;
+        if (phased) to_phase_tables(host, phases, per_slot, first);
+        const std::vector<wq::PhaseDev>& ph = phased ? per_slot : phases;
         cudaError_t e = cudaMemcpy(tab.proj + r.begin, host.data(),
                                    host.size() * sizeof(wq::ProjDev), cudaMemcpyHostToDevice);
         if (e == cudaSuccess)
-            e = cudaMemcpy(tab.phase + r.begin, phases.data(), phases.size() * sizeof(wq::PhaseDev),
+            e = cudaMemcpy(tab.phase + r.begin, ph.data(), ph.size() * sizeof(wq::PhaseDev),
                            cudaMemcpyHostToDevice);
         if (e != cudaSuccess) return wq::host_cuda_fail(e);
     }
@@ -236,7 +296,7 @@ wq_status_t upload_tables(const wq_proj_desc_t* projs, int count, void* base) {
 // of every run gets a completion threshold no launch reaches, so the
 // projections waiting for it run out their bounded waits.
 wq_status_t run_fused(const wq_proj_desc_t* projs, int count, void* workspace,
-                      size_t workspace_bytes, cudaStream_t s, void* tables,
+                      size_t workspace_bytes, cudaStream_t s, void* tables, bool phased,
                       bool stall_first_phase = false) {
     int sms = 0;
     if (wq_status_t st = wq::host_sm_count(&sms)) return st;
@@ -248,29 +308,41 @@ wq_status_t run_fused(const wq_proj_desc_t* projs, int count, void* workspace,
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     const Tables tab = tables_at(tables ? tables : ws + lay.table_off, count);
     std::vector<wq::ProjDev> host;
-    std::vector<wq::PhaseDev> phases;
+    std::vector<wq::PhaseDev> phases, per_slot;
+    std::vector<int> first;
+    bool prev_kernel = false;  // the last operation issued by this call was one of its kernels
     for (const Run& r : runs) {
         if (!r.fused) {
             if (wq_status_t st = run_single(projs[r.begin], workspace, workspace_bytes, s)) return st;
+            prev_kernel = launches_kernel(projs[r.begin]);
             continue;
         }
         long long units = 0;
         bool waits = false;
         if (wq_status_t st = build_table(projs, r, host, phases, &units, &waits)) return st;
         if (stall_first_phase && phases.size() > 1) phases[0].need = 0x7fffffff;
+        if (phased) to_phase_tables(host, phases, per_slot, first);
         if (!tables) {
             // pageable sources: each copy is staged before the call returns
+            const std::vector<wq::PhaseDev>& ph = phased ? per_slot : phases;
             cudaError_t e = cudaMemcpyAsync(tab.proj + r.begin, host.data(),
                                             host.size() * sizeof(wq::ProjDev),
                                             cudaMemcpyHostToDevice, s);
             if (e == cudaSuccess)
-                e = cudaMemcpyAsync(tab.phase + r.begin, phases.data(),
-                                    phases.size() * sizeof(wq::PhaseDev), cudaMemcpyHostToDevice, s);
+                e = cudaMemcpyAsync(tab.phase + r.begin, ph.data(),
+                                    ph.size() * sizeof(wq::PhaseDev), cudaMemcpyHostToDevice, s);
             if (e != cudaSuccess) return wq::host_cuda_fail(e);
+            prev_kernel = false;
+        }
+        if (phased) {
+            if (wq_status_t st = launch_phases(r, tab, phases, first, ws, lay, sms, s, prev_kernel))
+                return st;
+            continue;
         }
         if (wq_status_t st = launch_run(r, tab, static_cast<int>(phases.size()), units, waits,
                                         ws, lay, sms, s))
             return st;
+        prev_kernel = false;  // a fused run's launch follows its counters' reset, not a kernel
     }
     return WQ_OK;
 }
@@ -303,9 +375,12 @@ size_t wq_step_workspace_bytes(const wq_proj_desc_t* projs, int count, unsigned 
 wq_status_t wq_step_run_ex(const wq_proj_desc_t* projs, int count, unsigned flags,
                            void* workspace, size_t workspace_bytes, void* stream) {
     if (wq_status_t st = check_all(projs, count)) return st;
-    if (flags & ~WQ_STEP_FUSED) return WQ_ERR_INVALID_ARG;
+    if (flags & ~(WQ_STEP_FUSED | WQ_STEP_PHASES)) return WQ_ERR_INVALID_ARG;
+    if ((flags & WQ_STEP_PHASES) && !(flags & WQ_STEP_FUSED)) return WQ_ERR_INVALID_ARG;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (flags & WQ_STEP_FUSED) return run_fused(projs, count, workspace, workspace_bytes, s, nullptr);
+    if (flags & WQ_STEP_FUSED)
+        return run_fused(projs, count, workspace, workspace_bytes, s, nullptr,
+                         (flags & WQ_STEP_PHASES) != 0);
     return run_sequential(projs, count, workspace, workspace_bytes, s);
 }
 
@@ -320,14 +395,16 @@ wq_status_t wq_step_graph_create_ex(const wq_proj_desc_t* projs, int count, unsi
     if (!out || !workspace || count <= 0 || !projs) return WQ_ERR_INVALID_ARG;
     *out = nullptr;
     if (wq_status_t st = check_all(projs, count)) return st;
-    if (flags & ~WQ_STEP_FUSED) return WQ_ERR_INVALID_ARG;
+    if (flags & ~(WQ_STEP_FUSED | WQ_STEP_PHASES)) return WQ_ERR_INVALID_ARG;
+    if ((flags & WQ_STEP_PHASES) && !(flags & WQ_STEP_FUSED)) return WQ_ERR_INVALID_ARG;
+    const bool phased = (flags & WQ_STEP_PHASES) != 0;
     wq_step_graph* g = new (std::nothrow) wq_step_graph;
     if (!g) return WQ_ERR_CUDA;
     wq_status_t st = WQ_OK;
     if (flags & WQ_STEP_FUSED) {
         cudaError_t e = cudaMalloc(&g->tables, table_bytes(count));
         if (e != cudaSuccess) st = wq::host_cuda_fail(e);
-        if (st == WQ_OK) st = upload_tables(projs, count, g->tables);
+        if (st == WQ_OK) st = upload_tables(projs, count, g->tables, phased);
     }
     // Capture needs a non-legacy stream: use the caller's, or a private one.
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -341,7 +418,7 @@ wq_status_t wq_step_graph_create_ex(const wq_proj_desc_t* projs, int count, unsi
     if (st == WQ_OK) {
         wq_status_t run;
         if (flags & WQ_STEP_FUSED) {
-            run = run_fused(projs, count, workspace, workspace_bytes, s, g->tables);
+            run = run_fused(projs, count, workspace, workspace_bytes, s, g->tables, phased);
         } else {
             run = run_sequential(projs, count, workspace, workspace_bytes, s);
         }
@@ -392,7 +469,7 @@ wq_status_t wq_internal_step_stall_probe(const wq_proj_desc_t* projs, int count,
                                          size_t workspace_bytes, void* stream) {
     if (wq_status_t st = check_all(projs, count)) return st;
     return run_fused(projs, count, workspace, workspace_bytes,
-                     reinterpret_cast<cudaStream_t>(stream), nullptr, true);
+                     reinterpret_cast<cudaStream_t>(stream), nullptr, false, true);
 }
 
 }  // extern "C"
