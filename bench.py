@@ -56,7 +56,7 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU oracle sample budget")
     ap.add_argument("--layers", type=int, default=64)
     ap.add_argument("--profile-config", default=None,
-                    help="only run CALLS calls of this config (a seeded GEMM config, \"step\" or \"attention\"; for ncu captures)")
+                    help="only run CALLS calls of this config (a seeded GEMM config, \"step\", \"step-phased\" or \"attention\"; for ncu captures)")
     ap.add_argument("--calls", type=int, default=3)
     return ap.parse_args(argv)
 
@@ -710,7 +710,7 @@ def main_ours(args):
     sweep = []
     if not args.no_sweep:
         for M in synth.STEP_M_SWEEP:
-            r = run_sweep_point(stack, M, stream, max(3, args.steps // 4), 2, dist)
+            r = run_sweep_point(stack, M, stream, max(3, args.steps // 4), 2, dist, mode=head_mode)
             b = stack.step_bytes(M)
             ms = reduce_max(dist, r["ms_per_step"], device)
             sweep.append({"M": M, "ms_per_step": round(ms, 4),
@@ -855,17 +855,18 @@ def main_profile(args):
                           "bytes_per_call": attention_bytes(pa),
                           "max_abs_out": float(out.abs().max())}))
         return 0
-    if args.profile_config == "step":
+    if args.profile_config in ("step", "step-phased"):
         stack = StepStack(args.layers, device)
         _, _, _, descs = stack.buffers(args.m)
         cd = wq.make_descs(descs)
         ws = stack.fused_workspace(cd)
+        flags = wq.WQ_STEP_FUSED | (wq.WQ_STEP_PHASES if args.profile_config == "step-phased" else 0)
         for _ in range(args.calls):
-            wq.wq_step_run(cd, ws, flags=wq.WQ_STEP_FUSED)
+            wq.wq_step_run(cd, ws, flags=flags)
         torch.cuda.synchronize()
         wq.wq_check_workspace(ws)
         b = stack.step_bytes(args.m)
-        print(json.dumps({"profile_config": "step", "layers": args.layers, "M": args.m,
+        print(json.dumps({"profile_config": args.profile_config, "layers": args.layers, "M": args.m,
                           "calls": args.calls, "bytes_per_call": b["total"]}))
         return 0
     p = synth.CONFIGS[args.profile_config]

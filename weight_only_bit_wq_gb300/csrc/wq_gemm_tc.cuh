@@ -654,7 +654,10 @@ __device__ __forceinline__ void store_final(const ProjView& v, int n, const floa
 //   of their shares, so they have usually all arrived already.  Then the
 //   warp checks the counter first and, if they have, sums at once without
 //   publishing its own partial (two round trips fewer at the end of a share).
-template <int EPI, int NC>
+//   PAIR: two contributors' partials in flight at a time in the 16-row sum
+//   (measured faster in the single-projection and per-phase builds, slower in
+//   the fused build, which sits at the register ceiling).
+template <int EPI, int NC, bool PAIR>
 __device__ __forceinline__ void finish_rows(const Ctx& c, const ProjView& v,
                                             float (&acc)[NC], int t, bool whole,
                                             bool likely_last, int r, int q, int lane) {
@@ -705,24 +708,51 @@ __device__ __forceinline__ void finish_rows(const Ctx& c, const ProjView& v,
     }
     __syncwarp();  // the other lanes' reads follow lane 0's acquire
     if constexpr (NC == 16) {
-        // all contributors in k order (this warp's own sums in place of its partial)
+        // all contributors in k order (this warp's own sums in place of its
+        // partial), one or (PAIR) two contributors' partials in flight at a time
         float tot[NC];
 #pragma unroll
         for (int j = 0; j < NC; ++j) tot[j] = 0.f;
-        for (int b = b_first; b <= b_last; ++b) {
-            if (b == me) {
+        if constexpr (PAIR) {
+            for (int b = b_first; b <= b_last; b += 2) {
+                const bool two = b + 1 <= b_last;
+                const bool own0 = b == me, own1 = two && b + 1 == me;
+                // contributors after the first publish into their slot 0
+                const float* s0 = c.partials +
+                                  static_cast<size_t>(2 * b + (b == b_first ? first_role : 0)) *
+                                      (kMaxCols * kBN) +
+                                  r;
+                const float* s1 =
+                    c.partials + static_cast<size_t>(2 * (b + 1)) * (kMaxCols * kBN) + r;
+                float p0[NC], p1[NC];
 #pragma unroll
-                for (int j = 0; j < NC; ++j) tot[j] += acc[j];
-            } else {
-                const float* src = c.partials +
-                                   static_cast<size_t>(2 * b + (b == b_first ? first_role : 0)) *
-                                       (kMaxCols * kBN) +
-                                   r;
-                float part[NC];
+                for (int j = 0; j < NC; ++j) {
+                    p0[j] = (!own0 && j < v.M) ? __ldcg(s0 + j * kBN) : 0.f;
+                    p1[j] = (two && !own1 && j < v.M) ? __ldcg(s1 + j * kBN) : 0.f;
+                }
 #pragma unroll
-                for (int j = 0; j < NC; ++j) part[j] = j < v.M ? __ldcg(src + j * kBN) : 0.f;
+                for (int j = 0; j < NC; ++j) tot[j] += own0 ? acc[j] : p0[j];
+                if (two) {
 #pragma unroll
-                for (int j = 0; j < NC; ++j) tot[j] += part[j];
+                    for (int j = 0; j < NC; ++j) tot[j] += own1 ? acc[j] : p1[j];
+                }
+            }
+        } else {
+            for (int b = b_first; b <= b_last; ++b) {
+                if (b == me) {
+#pragma unroll
+                    for (int j = 0; j < NC; ++j) tot[j] += acc[j];
+                } else {
+                    const float* src = c.partials +
+                                       static_cast<size_t>(2 * b + (b == b_first ? first_role : 0)) *
+                                           (kMaxCols * kBN) +
+                                       r;
+                    float part[NC];
+#pragma unroll
+                    for (int j = 0; j < NC; ++j) part[j] = j < v.M ? __ldcg(src + j * kBN) : 0.f;
+#pragma unroll
+                    for (int j = 0; j < NC; ++j) tot[j] += part[j];
+                }
             }
         }
         store_final<EPI, NC>(v, n, tot, lane);
@@ -876,7 +906,7 @@ __device__ __forceinline__ void unpack_warp(const Ctx& c, uint32_t smem_u32, B& 
 // Epilogue warp (lane quarter q).  Per unit it reads the unit's two batches
 // of accumulators back (adding scale * D to the row's NC fp32 sums) and ends
 // tile segments.
-template <int BITS, int G, int NC, int EPI, class B>
+template <int BITS, int G, int NC, int EPI, bool PAIR, class B>
 __device__ __forceinline__ void epilogue_warp(const Ctx& c, B& bars, uint32_t tmem,
                                               volatile int* abort_flag, int q, int lane,
                                               int n_units) {
@@ -965,7 +995,7 @@ __device__ __forceinline__ void epilogue_warp(const Ctx& c, B& bars, uint32_t tm
         const bool end = tile_end || cc.last_of_share();
         if (end) {
             if (!dead)
-                finish_rows<EPI, NC>(c, cc.v, acc, cc.t, seg_from_start && tile_end,
+                finish_rows<EPI, NC, PAIR>(c, cc.v, acc, cc.t, seg_from_start && tile_end,
                             seg_from_start && !tile_end, r, q, lane);
 #pragma unroll
             for (int j = 0; j < NC; ++j) acc[j] = 0.f;
@@ -1368,7 +1398,7 @@ __global__ void __launch_bounds__(Lay<BITS, G, NC>::kThreads, 1)
 
     if (warp >= L::kUW) {
         // ------------------------------------------------------------ epilogue
-        epilogue_warp<BITS, G, NC, EPI>(c, bars, tmem, abort_flag, warp & 3, lane, n_units);
+        epilogue_warp<BITS, G, NC, EPI, HOLD>(c, bars, tmem, abort_flag, warp & 3, lane, n_units);
     } else if constexpr (BITS == 3) {
         // ------------------------------------------------------------ unpack
         static_for<0, L::kSplit>([&](auto hc) {
