@@ -93,6 +93,8 @@ struct StepArgs {
     int pdl;              // launched as a programmatic dependent of the previous kernel on the
                           // stream (one phase, nothing waits): X is read, and anything written,
                           // once that kernel completed
+    int act;              // with pdl: some projection of the launch asks for the activation
+                          // epilogue (otherwise the build without it serves)
 };
 
 // Static stream-K schedule: CTA b owns units [unit_begin(b), unit_begin(b+1)).

@@ -213,10 +213,14 @@ wq_status_t launch_run(const Run& r, Tables tab, int nphase, long long units, bo
 
 // One launch per phase of a run (tables from to_phase_tables); every launch
 // that follows another kernel of the step is a programmatic dependent one.
-wq_status_t launch_phases(const Run& r, Tables tab, const std::vector<wq::PhaseDev>& phases,
-                          const std::vector<int>& first, uint8_t* ws, const FusedLayout& lay,
-                          int sms, cudaStream_t s, bool& prev_kernel) {
+wq_status_t launch_phases(const wq_proj_desc_t* projs, const Run& r, Tables tab,
+                          const std::vector<wq::PhaseDev>& phases, const std::vector<int>& first,
+                          uint8_t* ws, const FusedLayout& lay, int sms, cudaStream_t s,
+                          bool& prev_kernel) {
     for (size_t p = 0; p < phases.size(); ++p) {
+        bool act = false;
+        for (int li = first[p]; li < first[p + 1]; ++li)
+            act = act || projs[r.begin + li].epilogue == WQ_EPI_SWIGLU;
         wq::StepArgs sa{};
         sa.proj = tab.proj + r.begin + first[p];
         sa.phase = tab.phase + r.begin + first[p];
@@ -229,6 +233,7 @@ wq_status_t launch_phases(const Run& r, Tables tab, const std::vector<wq::PhaseD
         sa.U = phases[p].U;
         sa.P = static_cast<int>(std::min<long long>(sms, phases[p].U));
         sa.pdl = prev_kernel ? 1 : 0;
+        sa.act = act ? 1 : 0;
         cudaError_t e;
         if (r.bits == 4)
             e = wq::launch_step_b4(r.group, sa, false, r.nc, s);
@@ -335,7 +340,8 @@ wq_status_t run_fused(const wq_proj_desc_t* projs, int count, void* workspace,
             prev_kernel = false;
         }
         if (phased) {
-            if (wq_status_t st = launch_phases(r, tab, phases, first, ws, lay, sms, s, prev_kernel))
+            if (wq_status_t st =
+                    launch_phases(projs, r, tab, phases, first, ws, lay, sms, s, prev_kernel))
                 return st;
             continue;
         }
