@@ -95,7 +95,7 @@ namespace wq {
 
 int choose_grid(int T, int I, int sm_count) {
     const long long U = static_cast<long long>(T) * I;
-    long long P = sm_count;
+    long long P = gemm_sm_budget(sm_count);
     if (P > U) P = U;
     const long long cap = static_cast<long long>(T) * kMaxSplit;
     if (P > cap) P = cap;

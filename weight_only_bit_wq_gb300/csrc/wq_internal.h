@@ -97,6 +97,21 @@ struct StepArgs {
                           // epilogue (otherwise the build without it serves)
 };
 
+// SMs a GEMM grid leaves free.  A launch that is a programmatic dependent of
+// the one before places its CTAs as that launch's CTAs leave their SMs; with
+// one CTA per SM the last of them could start only when the slowest CTA of
+// the previous launch had exited, after the dependency resolved, with none
+// of its packed words loaded, and so ended every launch of a chain last
+// (the same CTA index, launch after launch).  A grid of two CTAs fewer than
+// SMs lets every CTA start early (one or four fewer measured slower); the
+// single projection and the fused launch take the same grid, so that every
+// mode splits a projection alike.
+#ifndef WQ_SPARE_SMS
+#define WQ_SPARE_SMS 2
+#endif
+constexpr int kSpareSms = WQ_SPARE_SMS;
+inline int gemm_sm_budget(int sms) { return sms > kSpareSms ? sms - kSpareSms : 1; }
+
 // Static stream-K schedule: CTA b owns units [unit_begin(b), unit_begin(b+1)).
 inline long long unit_begin(long long U, int P, int b) { return U * b / P; }
 

@@ -200,7 +200,7 @@ wq_status_t launch_run(const Run& r, Tables tab, int nphase, long long units, bo
     sa.done = done;
     sa.err = reinterpret_cast<int*>(ws);
     sa.U = units;
-    sa.P = static_cast<int>(std::min<long long>(sms, units));
+    sa.P = static_cast<int>(std::min<long long>(wq::gemm_sm_budget(sms), units));
     sa.pdl = 0;
     if (r.bits == 4)
         e = wq::launch_step_b4(r.group, sa, waits, r.nc, s);
@@ -231,7 +231,7 @@ wq_status_t launch_phases(const wq_proj_desc_t* projs, const Run& r, Tables tab,
         sa.done = reinterpret_cast<int*>(ws + lay.done_off);
         sa.err = reinterpret_cast<int*>(ws);
         sa.U = phases[p].U;
-        sa.P = static_cast<int>(std::min<long long>(sms, phases[p].U));
+        sa.P = static_cast<int>(std::min<long long>(wq::gemm_sm_budget(sms), phases[p].U));
         sa.pdl = prev_kernel ? 1 : 0;
         sa.act = act ? 1 : 0;
         cudaError_t e;
