@@ -385,6 +385,66 @@ def run_sweep_point(stack, M, stream, steps, warmup, dist, clocks=None, e2e=Fals
     return out
 
 
+E2E_CHUNK_LAYERS = 8  # layers per copy/compute chunk of the end-to-end step
+
+
+def run_e2e_pipelined(stack, M, stream, steps, warmup, dist, mode, chunk_layers=E2E_CHUNK_LAYERS):
+    """ms per step end to end through the C ABI: every step copies all X from pinned host
+    memory and reads all Y back, chunk by chunk (chunk_layers layers each) on two copy
+    streams, so that a chunk's copies overlap the step graphs of the other chunks.  Each
+    chunk is its own step graph in the headline's mode; stream order carries the layer
+    chain from one chunk to the next."""
+    import torch
+
+    wq = stack.wq
+    x_host, x_dev, y_dev, descs = stack.buffers(M)
+    y_host = torch.empty(y_dev.numel(), dtype=torch.float32).pin_memory()
+    flags = {"fused": wq.WQ_STEP_FUSED, "phased": wq.WQ_STEP_FUSED | wq.WQ_STEP_PHASES,
+             "sequential": 0}[mode]
+    per = 6 * chunk_layers
+    stream.wait_stream(torch.cuda.current_stream())
+    chunks, xo, yo = [], 0, 0
+    for c0 in range(0, len(descs), per):
+        sub = [dict(d) for d in descs[c0:c0 + per]]
+        for d in sub:  # dependencies on earlier chunks are met by stream order
+            d["after"] = d["after"] - c0 if d["after"] >= c0 else -1
+        nx = sum(d["M"] * d["K"] for d in sub)
+        ny = sum(d["M"] * d["N"] for d in sub)
+        cd = wq.make_descs(sub)
+        ws = stack.ws if mode == "sequential" else stack.fused_workspace(cd)
+        chunks.append((wq.StepGraph(cd, ws, stream=stream, flags=flags), xo, nx, yo, ny, ws))
+        xo += nx
+        yo += ny
+    h2d, d2h = torch.cuda.Stream(stack.device), torch.cuda.Stream(stack.device)
+    ev_x = [torch.cuda.Event() for _ in chunks]
+    ev_c = [torch.cuda.Event() for _ in chunks]
+    ev_y = [torch.cuda.Event() for _ in chunks]
+
+    def step():
+        h2d.wait_stream(stream)  # after the step's start (and the previous step's graphs)
+        for i, (_, xo, nx, _, _, _) in enumerate(chunks):
+            with torch.cuda.stream(h2d):
+                x_dev[xo:xo + nx].copy_(x_host[xo:xo + nx], non_blocking=True)
+            ev_x[i].record(h2d)
+        for i, (g, _, _, yo, ny, _) in enumerate(chunks):
+            stream.wait_event(ev_x[i])
+            g.launch(stream=stream)
+            ev_c[i].record(stream)
+            d2h.wait_event(ev_c[i])
+            with torch.cuda.stream(d2h):
+                y_host[yo:yo + ny].copy_(y_dev[yo:yo + ny], non_blocking=True)
+            ev_y[i].record(d2h)
+        stream.wait_event(ev_y[-1])  # the step ends when its last Y is on the host
+
+    ms = time_launches(step, stream, steps, warmup, dist)
+    torch.cuda.synchronize()
+    for g, *_, ws in chunks:
+        wq.wq_check_workspace(ws, stream=stream)
+        g.close()
+    return {"e2e_ms": ms, "h2d_bytes": x_host.numel() * 2, "d2h_bytes": y_host.numel() * 4,
+            "chunks": len(chunks)}
+
+
 def run_dominant(stack, M, stream, steps, warmup, dist):
     """ms per launch of the dominant projection (fused gate/up), 64 launches per graph."""
     import torch
@@ -705,7 +765,9 @@ def main_ours(args):
     head = heads[head_mode]
     sb = stack.step_bytes(args.m)
     value, ms_max, packed_all = whole_job_gbs(dist, sb["packed"], head["ms_per_step"], device)
-    e2e_max = reduce_max(dist, head["e2e_ms"], device)
+    serial_e2e_max = reduce_max(dist, head["e2e_ms"], device)
+    pipe = run_e2e_pipelined(stack, args.m, stream, max(3, args.steps // 2), 2, dist, head_mode)
+    e2e_max = reduce_max(dist, pipe["e2e_ms"], device)
 
     sweep = []
     if not args.no_sweep:
@@ -782,9 +844,15 @@ def main_ours(args):
             "step_modes": modes, "single_launch": single, "attention": attention,
             "cpu_baseline": cpu,
             "e2e": {"value": round(packed_all / (e2e_max * 1e-3) / 1e9, 1), "unit": "GB/s",
-                    "h2d_bytes_per_step": head["h2d_bytes"], "d2h_bytes_per_step": head["d2h_bytes"],
+                    "h2d_bytes_per_step": pipe["h2d_bytes"], "d2h_bytes_per_step": pipe["d2h_bytes"],
                     "ms_per_step": round(e2e_max, 4),
-                    "how": "pinned host X -> device, step graph via the C ABI, device Y -> pinned host"},
+                    "how": (f"every step: all X from pinned host memory to the device and all Y "
+                            f"back, in {pipe['chunks']} chunks of {E2E_CHUNK_LAYERS} layers on two "
+                            f"copy streams overlapping the other chunks' step graphs (the headline's "
+                            f"mode, launched through the C ABI); the step ends when its last Y is "
+                            f"on the host"),
+                    "serial_ms_per_step": round(serial_e2e_max, 4),
+                    "serial_how": "all X to the device, then the whole step graph, then all Y back"},
             "gpu_launches": head["launches_per_step"] * args.steps,
             "clocks": clock_info, "sweep": sweep, "configs": configs,
         }

@@ -112,6 +112,14 @@ wq_status_t wq_dequant(const uint32_t* wq, const uint16_t* scales, const uint8_t
  */
 size_t wq_workspace_bytes(int M, int N, int K, int group, int bits);
 
+/*
+ * The same for a device with sm_count SMs (sm_count > 0), whether or not it
+ * is the current one: a workspace sized for sm_count serves every device
+ * with at most that many SMs.  Host arithmetic only (no CUDA call).  Returns
+ * 0 for bad arguments.  No passage of the pages defines it.
+ */
+size_t wq_workspace_bytes_for(int M, int N, int K, int group, int bits, int sm_count);
+
 /* Zero a caller-owned workspace (required once before its first use; every
  * wq_gemm call leaves it zeroed again). */
 wq_status_t wq_workspace_init(void* workspace, size_t workspace_bytes, void* stream);

@@ -34,11 +34,29 @@ def test_every_declared_symbol_is_exported(wq):
 
 
 def test_abi_version_and_words(wq):
-    assert wq.abi_version() == 103
+    assert wq.abi_version() == 104
     assert wq.wq_packed_words_per_row(17408, 3) == 1744
     assert wq.wq_packed_words_per_row(5120, 4) == 640
     assert wq.wq_packed_words_per_row(17408, 2) == 1088
     assert wq.wq_packed_words_per_row(10, 5) == -1
+
+
+def test_workspace_bytes_for_any_sm_count(wq):
+    f = wq.wq_workspace_bytes_for
+    n = f(16, 5120, 5120, 128, 4, 152)
+    # split-K partial slots (two per CTA, 32 x 128 fp32 each) and 16 arrival
+    # counters per 128-row tile, in whole 256-byte blocks
+    assert n % 256 == 0
+    assert n >= 2 * 152 * 32 * 128 * 4 + 40 * 16 * 4
+    assert f(1, 5120, 5120, 128, 4, 152) == n          # never depends on M
+    assert f(16, 5120, 17408, 128, 4, 152) == n        # nor on K
+    assert f(16, 5120, 5120, 32, 2, 152) == n          # nor on the format
+    assert f(16, 5120, 5120, 128, 4, 76) < n < f(16, 5120, 5120, 128, 4, 304)
+    assert f(16, 34816, 5120, 128, 4, 152) > n         # more tiles, more counters
+    for bad in ((16, 5120, 5120, 128, 4, 0), (16, 5120, 5120, 128, 5, 152),
+                (33, 5120, 5120, 128, 4, 152), (16, 5120, 100, 32, 4, 152),
+                (16, -1, 5120, 128, 4, 152)):
+        assert f(*bad) == 0, bad
 
 
 def _gemm(lib, M=4, N=8, K=128, group=128, bits=4, x=16, w=16, s=16, z=16, y=16):

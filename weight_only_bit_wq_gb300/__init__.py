@@ -23,7 +23,7 @@ LIB_PATH = os.path.join(_HERE, "libwq.so")
 WQ_OK, WQ_ERR_INVALID_ARG, WQ_ERR_UNSUPPORTED, WQ_ERR_CUDA, WQ_ERR_TIMEOUT = range(5)
 
 EXPORTED = ("wq_abi_version", "wq_status_string", "wq_last_cuda_error", "wq_packed_words_per_row",
-            "wq_pack", "wq_unpack", "wq_dequant", "wq_workspace_bytes", "wq_workspace_init",
+            "wq_pack", "wq_unpack", "wq_dequant", "wq_workspace_bytes", "wq_workspace_bytes_for", "wq_workspace_init",
             "wq_gemm", "wq_gemm_swiglu", "wq_check_workspace", "wq_gemm_noalloc", "wq_check_noalloc",
             "wq_step_workspace_bytes", "wq_step_run",
             "wq_step_run_ex", "wq_step_graph_create", "wq_step_graph_create_ex",
@@ -73,6 +73,7 @@ def _lib() -> ctypes.CDLL:
             "wq_unpack": ([P, P, I, I, I, P], I),
             "wq_dequant": ([P, P, P, P, I, I, I, I, P], I),
             "wq_workspace_bytes": ([I, I, I, I, I], S),
+            "wq_workspace_bytes_for": ([I, I, I, I, I, I], S),
             "wq_workspace_init": ([P, S, P], I),
             "wq_gemm": ([P, P, P, P, P, I, I, I, I, I, P, S, P], I),
             "wq_gemm_swiglu": ([P, P, P, P, P, I, I, I, I, I, P, S, P], I),
@@ -156,6 +157,10 @@ def wq_dequant(wq, scales, zeros, K: int, group: int, bits: int, out=None, strea
 
 def wq_workspace_bytes(M: int, N: int, K: int, group: int, bits: int) -> int:
     return int(_lib().wq_workspace_bytes(M, N, K, group, bits))
+
+
+def wq_workspace_bytes_for(M: int, N: int, K: int, group: int, bits: int, sm_count: int) -> int:
+    return int(_lib().wq_workspace_bytes_for(M, N, K, group, bits, sm_count))
 
 
 def wq_workspace_init(ws: torch.Tensor, stream=None) -> torch.Tensor:

@@ -106,7 +106,7 @@ int choose_grid(int T, int I, int sm_count) {
 
 extern "C" {
 
-int wq_abi_version(void) { return 103; }
+int wq_abi_version(void) { return 104; }
 
 const char* wq_status_string(wq_status_t s) {
     switch (s) {
@@ -179,6 +179,14 @@ size_t wq_workspace_bytes(int M, int N, int K, int group, int bits) {
     if (device_info(&d) != WQ_OK) return 0;
     const int T = (N + wq::kBN - 1) / wq::kBN;
     return ws_layout(T, d->sm_count).bytes;
+}
+
+size_t wq_workspace_bytes_for(int M, int N, int K, int group, int bits, int sm_count) {
+    if (!valid_bits(bits) || !valid_group(group) || M < 0 || M > wq::kMaxCols || N < 0 || K < 0 ||
+        K % group != 0 || sm_count <= 0)
+        return 0;
+    const int T = (N + wq::kBN - 1) / wq::kBN;
+    return ws_layout(T, sm_count).bytes;
 }
 
 wq_status_t wq_workspace_init(void* workspace, size_t bytes, void* stream) {
