@@ -265,9 +265,12 @@ typedef struct wq_proj_desc {
  * persistent launch over all of that phase's projections, and stream order --
  * every launch after the first a programmatic dependent of the one before --
  * replaces the device-side waits between phases.  Independent projections of a
- * phase still share one launch and one stream-K split.  Results as
- * WQ_STEP_FUSED (the split of each phase is the same).  Not part of the pages:
- * a launch plan for the same step. */
+ * phase still share one launch and one stream-K split.  Each launch takes a
+ * grid whose shares fall on tile boundaries where one lies near the SM count,
+ * so its split can differ from WQ_STEP_FUSED's: results agree with the fused
+ * launch to rounding; a row alone is still bit-identical to the same row
+ * stacked, and repeated steps are bit-identical.  Not part of the pages: a
+ * launch plan for the same step. */
 #define WQ_STEP_PHASES 2u
 
 /* Workspace bytes for a step in the given mode (0 for invalid input).  In

@@ -10,10 +10,11 @@ random rows; the oracle recomputes those rows from the same seeded generator),
 at 16 rows (the benchmark's row count), 1 row and 24 rows (the 32-row kernel
 build).  Rows are bitwise equal across the three row counts (batch
 invariance: OpenJet news page, "新提示不会让所有人停摆").  The sequential mode
-(one launch per projection) is checked against the oracle on the same rows; it
-splits each tile's K range differently from the fused launch, so the two agree
-to rounding, not bit for bit.  One launch per dependency phase gives the fused
-launch's results bit for bit.
+(one launch per projection) and the per-phase mode (one launch per dependency
+phase, the bench's headline) are checked against the oracle on the same rows;
+they split each tile's K range differently from the fused launch, so the modes
+agree to rounding, not bit for bit.  The per-phase mode is also bitwise
+batch-invariant (16 rows against 1).
 """
 import numpy as np
 import pytest
@@ -119,8 +120,11 @@ def test_sequential_and_phased_full_size_all_projections(stack):
     import weight_only_bit_wq_gb300 as wq
     ys = _run(wq, stack, 16, 0)
     _check_oracle(stack, ys, 16, "sequential")
-    # one launch per dependency phase: the fused launch's split, bit for bit
-    fused = _run(wq, stack, 16, wq.WQ_STEP_FUSED)
-    phased = _run(wq, stack, 16, wq.WQ_STEP_FUSED | wq.WQ_STEP_PHASES)
-    for i, (a, b) in enumerate(zip(fused, phased)):
-        assert np.array_equal(a.view(np.uint32), b.view(np.uint32)), i
+    # one launch per dependency phase (the headline mode), at 16 rows and 1 row
+    flags = wq.WQ_STEP_FUSED | wq.WQ_STEP_PHASES
+    p16 = _run(wq, stack, 16, flags)
+    _check_oracle(stack, p16, 16, "phased")
+    p1 = _run(wq, stack, 1, flags)
+    _check_oracle(stack, p1, 1, "phased")
+    for i, (a, b) in enumerate(zip(p16, p1)):
+        assert np.array_equal(b[0].view(np.uint32), a[0].view(np.uint32)), i

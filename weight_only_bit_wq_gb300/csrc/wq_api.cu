@@ -93,9 +93,24 @@ cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 
 namespace wq {
 
+int aligned_grid(int T, int budget, bool split_tiles) {
+    if (T <= 0 || budget <= 0) return budget;
+    const int lo = budget * 74 / 100;
+    if (T <= budget) {
+        const int k = budget / T;
+        return split_tiles && k * T >= lo ? k * T : budget;
+    }
+    for (int P = budget; P >= lo && P > 0; --P)
+        if (T % P == 0) return P;
+    return budget;
+}
+
+// Measured on 34,816 x 5,120 at 12 rows: 136 CTAs of two whole tiles each run
+// in 23.9 us against 25.3 us for 150 CTAs with split tiles (3-bit: 32.2
+// against 36.6 us).
 int choose_grid(int T, int I, int sm_count) {
     const long long U = static_cast<long long>(T) * I;
-    long long P = gemm_sm_budget(sm_count);
+    long long P = aligned_grid(T, gemm_sm_budget(sm_count), false);
     if (P > U) P = U;
     const long long cap = static_cast<long long>(T) * kMaxSplit;
     if (P > cap) P = cap;

@@ -118,6 +118,13 @@ inline long long unit_begin(long long U, int P, int b) { return U * b / P; }
 // Grid size from (N, K, bits) and the SM count only (never from M).
 int choose_grid(int T, int I, int sm_count);
 
+// At most `budget` CTAs for T tiles whose stream-K shares start and end on
+// tile boundaries, if such a grid lies within 74 % of the budget: whole tiles
+// per CTA (the largest divisor of T), or, with split_tiles, k CTAs per tile
+// (k T, the largest such); else the budget.  A share that ends inside a tile
+// ends with a split-K fix-up, the slowest part of a launch's tail.
+int aligned_grid(int T, int budget, bool split_tiles);
+
 // Tensor-core (tcgen05) GEMM kernels, one translation unit per bit width.
 cudaError_t launch_gemm_tc_b4(int group, const CUtensorMap& tmW, const CUtensorMap& tmX,
                               const GemmArgs& a, cudaStream_t s);

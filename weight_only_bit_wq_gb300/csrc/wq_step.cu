@@ -215,8 +215,8 @@ wq_status_t launch_run(const Run& r, Tables tab, int nphase, long long units, bo
 // that follows another kernel of the step is a programmatic dependent one.
 wq_status_t launch_phases(const wq_proj_desc_t* projs, const Run& r, Tables tab,
                           const std::vector<wq::PhaseDev>& phases, const std::vector<int>& first,
-                          uint8_t* ws, const FusedLayout& lay, int sms, cudaStream_t s,
-                          bool& prev_kernel) {
+                          const std::vector<wq::ProjDev>& host, uint8_t* ws,
+                          const FusedLayout& lay, int sms, cudaStream_t s, bool& prev_kernel) {
     for (size_t p = 0; p < phases.size(); ++p) {
         bool act = false;
         for (int li = first[p]; li < first[p + 1]; ++li)
@@ -231,7 +231,21 @@ wq_status_t launch_phases(const wq_proj_desc_t* projs, const Run& r, Tables tab,
         sa.done = reinterpret_cast<int*>(ws + lay.done_off);
         sa.err = reinterpret_cast<int*>(ws);
         sa.U = phases[p].U;
-        sa.P = static_cast<int>(std::min<long long>(wq::gemm_sm_budget(sms), phases[p].U));
+        // a grid whose shares fall on tile boundaries where the phase's tiles
+        // all have the same number of units (measured on the layer chain:
+        // q/k/v on 112 CTAs, o and down on 120, gate/up on 136 instead of 150
+        // each, 3 % faster)
+        int T = 0, I = -1;
+        bool uniform_i = true;
+        for (int li = first[p]; li < first[p + 1]; ++li) {
+            const wq::ProjDev& d = host[static_cast<size_t>(li)];
+            T += d.T;
+            if (I < 0) I = d.I;
+            else if (d.I != I) uniform_i = false;
+        }
+        const int budget = wq::gemm_sm_budget(sms);
+        const int Pa = uniform_i ? wq::aligned_grid(T, budget, true) : budget;
+        sa.P = static_cast<int>(std::min<long long>(Pa, phases[p].U));
         sa.pdl = prev_kernel ? 1 : 0;
         sa.act = act ? 1 : 0;
         cudaError_t e;
@@ -341,7 +355,7 @@ wq_status_t run_fused(const wq_proj_desc_t* projs, int count, void* workspace,
         }
         if (phased) {
             if (wq_status_t st =
-                    launch_phases(projs, r, tab, phases, first, ws, lay, sms, s, prev_kernel))
+                    launch_phases(projs, r, tab, phases, first, host, ws, lay, sms, s, prev_kernel))
                 return st;
             continue;
         }
