@@ -58,6 +58,8 @@ def parse_args(argv=None):
     ap.add_argument("--profile-config", default=None,
                     help="only run CALLS calls of this config (a seeded GEMM config, \"step\", \"step-phased\" or \"attention\"; for ncu captures)")
     ap.add_argument("--calls", type=int, default=3)
+    ap.add_argument("--e2e-chunk-layers", type=int, default=8,
+                    help="layers per copy/compute chunk of the end-to-end step")
     return ap.parse_args(argv)
 
 
@@ -385,10 +387,7 @@ def run_sweep_point(stack, M, stream, steps, warmup, dist, clocks=None, e2e=Fals
     return out
 
 
-E2E_CHUNK_LAYERS = 8  # layers per copy/compute chunk of the end-to-end step
-
-
-def run_e2e_pipelined(stack, M, stream, steps, warmup, dist, mode, chunk_layers=E2E_CHUNK_LAYERS):
+def run_e2e_pipelined(stack, M, stream, steps, warmup, dist, mode, chunk_layers=8):
     """ms per step end to end through the C ABI: every step copies all X from pinned host
     memory and reads all Y back, chunk by chunk (chunk_layers layers each) on two copy
     streams, so that a chunk's copies overlap the step graphs of the other chunks.  Each
@@ -766,7 +765,8 @@ def main_ours(args):
     sb = stack.step_bytes(args.m)
     value, ms_max, packed_all = whole_job_gbs(dist, sb["packed"], head["ms_per_step"], device)
     serial_e2e_max = reduce_max(dist, head["e2e_ms"], device)
-    pipe = run_e2e_pipelined(stack, args.m, stream, max(3, args.steps // 2), 2, dist, head_mode)
+    pipe = run_e2e_pipelined(stack, args.m, stream, max(3, args.steps // 2), 2, dist, head_mode,
+                             chunk_layers=args.e2e_chunk_layers)
     e2e_max = reduce_max(dist, pipe["e2e_ms"], device)
 
     sweep = []
@@ -847,7 +847,7 @@ def main_ours(args):
                     "h2d_bytes_per_step": pipe["h2d_bytes"], "d2h_bytes_per_step": pipe["d2h_bytes"],
                     "ms_per_step": round(e2e_max, 4),
                     "how": (f"every step: all X from pinned host memory to the device and all Y "
-                            f"back, in {pipe['chunks']} chunks of {E2E_CHUNK_LAYERS} layers on two "
+                            f"back, in {pipe['chunks']} chunks of {args.e2e_chunk_layers} layers on two "
                             f"copy streams overlapping the other chunks' step graphs (the headline's "
                             f"mode, launched through the C ABI); the step ends when its last Y is "
                             f"on the host"),

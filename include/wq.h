@@ -281,7 +281,9 @@ size_t wq_step_workspace_bytes(const wq_proj_desc_t* projs, int count, unsigned 
 /* Run the step once.  Sequential mode accepts any workspace wq_gemm accepts
  * (NULL = the library buffer); fused mode needs `workspace` of at least
  * wq_step_workspace_bytes(), 16-byte aligned, zeroed once (wq_workspace_init)
- * before its first use. */
+ * before its first use.  Every launch leaves the workspace's counters zeroed,
+ * so one workspace serves, one step at a time on one stream, every descriptor
+ * set it is large enough for. */
 wq_status_t wq_step_run(const wq_proj_desc_t* projs, int count, void* workspace,
                         size_t workspace_bytes, void* stream);
 wq_status_t wq_step_run_ex(const wq_proj_desc_t* projs, int count, unsigned flags,

@@ -125,6 +125,29 @@ def test_fused_uniform_stack_matches_oracle(fmt, deps):
                     assert np.array_equal(y.view(np.uint32), r.view(np.uint32)), (flags, p.name)
 
 
+def test_fused_workspace_serves_smaller_and_larger_sets():
+    # The workspace layout depends on the descriptor set (the completion
+    # counters sit after the split-K counters of the set's tiles), so a smaller
+    # set's completion counters occupy a larger set's split-K counters: every
+    # launch must leave them zeroed.  One layer, then two, then one again, on
+    # one workspace sized for the two.
+    import weight_only_bit_wq_gb300 as wq
+    projs = _uniform_stack(5, 4, 128, layers=2)
+    refs = [oracle_gemm(p, w, x) for p, w, x, d in projs]
+    full = _descs(wq, projs, _layer_after(len(projs)))
+    part = _descs(wq, projs[:6], _layer_after(6))
+    ws = wq.new_step_workspace(full, wq.WQ_STEP_FUSED)
+    for descs, n in ((part, 6), (full, 12), (part, 6), (full, 12)):
+        for p, w, x, d in projs:
+            d["y"].fill_(float("nan"))
+        wq.wq_step_run(descs, ws, flags=wq.WQ_STEP_FUSED)
+        torch.cuda.synchronize()
+        wq.wq_check_workspace(ws)
+        for (p, w, x, d), r in zip(projs[:n], refs[:n]):
+            err = rel_err(d["y"].cpu().numpy(), r)
+            assert err <= REL_TOL and err <= ARITH_TOL, (n, p.name, err)
+
+
 @pytest.mark.parametrize("deps", [False, True], ids=["independent", "layer-chain"])
 @pytest.mark.parametrize("M", [1, 12])
 def test_fused_step_matches_oracle(M, deps):

@@ -72,6 +72,13 @@ Tables tables_at(void* base, int count) {
     return t;
 }
 
+// Workspace of a fused step: error word, split-K partials, split-K counters,
+// completion counters, projection tables.  The offsets depend on the
+// descriptor set (its tile and projection counts), so one set's completion
+// counters or tables can sit where another set's split-K counters are; every
+// call therefore leaves all of them zeroed (the kernel its split-K counters,
+// memsets after the launch the rest), and one workspace serves every set it is
+// large enough for.
 FusedLayout fused_layout(const wq_proj_desc_t* projs, int count, const std::vector<Run>& runs,
                          int sms) {
     size_t max_tiles = 0, max_count = 0;
@@ -208,6 +215,7 @@ wq_status_t launch_run(const Run& r, Tables tab, int nphase, long long units, bo
         e = wq::launch_step_b3(r.group, sa, waits, r.nc, s);
     else
         e = wq::launch_step_b2(r.group, sa, waits, r.nc, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(done, 0, static_cast<size_t>(n) * sizeof(int), s);
     return e == cudaSuccess ? WQ_OK : wq::host_cuda_fail(e);
 }
 
@@ -357,11 +365,21 @@ wq_status_t run_fused(const wq_proj_desc_t* projs, int count, void* workspace,
             if (wq_status_t st =
                     launch_phases(projs, r, tab, phases, first, host, ws, lay, sms, s, prev_kernel))
                 return st;
-            continue;
-        }
-        if (wq_status_t st = launch_run(r, tab, static_cast<int>(phases.size()), units, waits,
-                                        ws, lay, sms, s))
+        } else if (wq_status_t st = launch_run(r, tab, static_cast<int>(phases.size()), units,
+                                               waits, ws, lay, sms, s)) {
             return st;
+        }
+        if (!tables) {
+            // staged tables are zeroed again once the launches have read them
+            cudaError_t e = cudaMemsetAsync(tab.proj + r.begin, 0,
+                                            host.size() * sizeof(wq::ProjDev), s);
+            if (e == cudaSuccess)
+                e = cudaMemsetAsync(tab.phase + r.begin, 0,
+                                    (phased ? per_slot : phases).size() * sizeof(wq::PhaseDev), s);
+            if (e != cudaSuccess) return wq::host_cuda_fail(e);
+            prev_kernel = false;
+        }
+        if (phased) continue;
         prev_kernel = false;  // a fused run's launch follows its counters' reset, not a kernel
     }
     return WQ_OK;
