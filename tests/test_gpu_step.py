@@ -125,6 +125,47 @@ def test_fused_uniform_stack_matches_oracle(fmt, deps):
                     assert np.array_equal(y.view(np.uint32), r.view(np.uint32)), (flags, p.name)
 
 
+def _chain_outputs(wq, projs, M, flags, ws=None):
+    descs = wq.make_descs([dict(x=d["x"][:M], wq=d["wq"], scales=d["s"], zeros=d["z"],
+                                y=d["y"][:M], M=M, N=p.N, K=p.K, group=p.group, bits=p.bits,
+                                after=i - 1) for i, (p, w, x, d) in enumerate(projs)])
+    if ws is None:
+        ws = wq.new_step_workspace(descs, wq.WQ_STEP_FUSED)
+    for p, w, x, d in projs:
+        d["y"].fill_(float("nan"))
+    wq.wq_step_run(descs, ws, flags=flags)
+    torch.cuda.synchronize()
+    wq.wq_check_workspace(ws)
+    return [d["y"][:M].cpu().numpy() for p, w, x, d in projs], ws
+
+
+def test_phased_cluster_fixup_matches_oracle():
+    # Per-phase launches whose grid gives each tile k = 2..4 CTAs (here 40- and
+    # 56-tile projections on a 150-CTA budget: k = 3 and 2) run as one cluster
+    # per tile and add the split-K sums through shared memory.  A chain of one
+    # projection per phase, against the oracle, bitwise across repeats and
+    # across row counts.
+    import weight_only_bit_wq_gb300 as wq
+    shapes = [(2048, 5120), (5120, 5120), (1536, 7168), (17408, 5120)]  # (K, N)
+    M = 5
+    projs = []
+    for i, (K, N) in enumerate(shapes):
+        p = synth.Projection(f"c{i}", M, N, K, 4, 128, 500, index=i)
+        w, x, d = to_dev_host_inputs(p)
+        d["y"] = torch.empty((M, N), dtype=torch.float32, device=dev())
+        projs.append((p, w, x, d))
+    flags = wq.WQ_STEP_FUSED | wq.WQ_STEP_PHASES
+    ys, ws = _chain_outputs(wq, projs, M, flags)
+    for (p, w, x, d), y in zip(projs, ys):
+        err = rel_err(y, oracle_gemm(p, w, x))
+        assert err <= REL_TOL and err <= ARITH_TOL, (p.name, err)
+    again, _ = _chain_outputs(wq, projs, M, flags, ws)
+    one, _ = _chain_outputs(wq, projs, 1, flags, ws)
+    for a, b, c in zip(ys, again, one):
+        assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+        assert np.array_equal(a[:1].view(np.uint32), c.view(np.uint32))
+
+
 def test_fused_workspace_serves_smaller_and_larger_sets():
     # The workspace layout depends on the descriptor set (the completion
     # counters sit after the split-K counters of the set's tiles), so a smaller

@@ -138,6 +138,14 @@ struct Lay {
     static constexpr int kStages = clamp_tc(smem_budget_tc(NC) / kStageBytes, 2, 8);
     static constexpr int kBarOffset = kStages * kStageBytes;
     static constexpr int kSmemBytes = kBarOffset + 512 + 1024;  // barriers/flags + align slack
+    // Cluster builds (a tile's k <= kFixMaxK contributors in one cluster): the
+    // partials of ranks 1 .. k-1 land in rank 0's shared memory after the
+    // barriers, [rank - 1][row][NC] fp32.
+    static constexpr int kFixMaxK = 4;
+    static constexpr int kFixOff = kBarOffset + 512;
+    static constexpr int kFixBytes = (kFixMaxK - 1) * kBN * NC * 4;
+    static constexpr int kSmemBytesClu = kSmemBytes + kFixBytes;
+    static constexpr bool kCluOk = NC == 16 && kSmemBytesClu <= 232448;
     // Tensor memory: kNA batch slots of A tiles (plus zero-point tiles when
     // the zero point goes on the tensor core) and kND batch slots of fp32
     // accumulators, the largest plan that fits in 512 columns.
@@ -788,6 +796,55 @@ __device__ __forceinline__ void finish_rows(const Ctx& c, const ProjView& v,
     count_done();
 }
 
+// End of a tile segment in a cluster build: the launch gives each tile k
+// CTAs, ranks 0 .. k-1 of one cluster in k order, one segment each.  Ranks
+// 1 .. k-1 store their sums into rank 0's shared memory with asynchronous
+// stores that complete on rank 0's `fix` barrier, and are done; rank 0 waits
+// (bounded) for them and adds them to its own in rank order, i.e. in k order.
+// No global partials, no counters, no L2 round trips.
+//   fix_smem, fix_bar: this CTA's buffer and barrier (rank 0's are the ones used)
+template <int EPI, int NC>
+__device__ __forceinline__ void finish_rows_cluster(const Ctx& c, const ProjView& v,
+                                                    const float (&acc)[NC], int t, bool whole,
+                                                    int r, int lane, uint32_t fix_smem,
+                                                    uint64_t* fix_bar, uint32_t rank,
+                                                    uint32_t k, volatile int* abort_flag) {
+    static_assert(NC % 4 == 0, "whole float4 pieces");
+    const int n = t * kBN + r;
+    if (whole) {
+        store_final<EPI, NC>(v, n, acc, lane);
+        return;
+    }
+    if (rank != 0) {
+        const uint32_t dst =
+            map_to_rank(fix_smem + ((rank - 1) * kBN + static_cast<uint32_t>(r)) * NC * 4u, 0u);
+        const uint32_t bar = map_to_rank(smem_addr(fix_bar), 0u);
+#pragma unroll
+        for (int j = 0; j < NC; j += 4)
+            st_async_v4(dst + 4u * j, acc[j], acc[j + 1], acc[j + 2], acc[j + 3], bar);
+        return;
+    }
+    if (!__all_sync(kFull, mbar_wait_cluster(fix_bar, 0u, abort_flag))) {
+        if (lane == 0) record_error_tc(c.err, abort_flag);
+        return;
+    }
+    float tot[NC];
+#pragma unroll
+    for (int j = 0; j < NC; ++j) tot[j] = acc[j];
+    for (uint32_t b = 1; b < k; ++b) {
+        const uint32_t src = fix_smem + ((b - 1) * kBN + static_cast<uint32_t>(r)) * NC * 4u;
+#pragma unroll
+        for (int j = 0; j < NC; j += 4) {
+            const uint4 p = lds128(src + 4u * j);
+            tot[j] += __uint_as_float(p.x);
+            tot[j + 1] += __uint_as_float(p.y);
+            tot[j + 2] += __uint_as_float(p.z);
+            tot[j + 3] += __uint_as_float(p.w);
+        }
+    }
+    store_final<EPI, NC>(v, n, tot, lane);
+}
+
 // Shared-memory barriers of one CTA.
 template <int S, int NA, int ND>
 struct Bars {
@@ -799,6 +856,7 @@ struct Bars {
     uint64_t dfull[ND];  // accumulator slot's MMAs complete (tcgen05.commit)
     uint64_t dfree[ND];  // accumulator slot read back (epilogue warps)
     uint64_t drain;      // every MMA complete
+    uint64_t fix;        // cluster builds: the other contributors' partials landed
     uint32_t tmem_base;
     int abort_flag;
     int n_units;         // units of this CTA (all its phase shares)
@@ -906,10 +964,11 @@ __device__ __forceinline__ void unpack_warp(const Ctx& c, uint32_t smem_u32, B& 
 // Epilogue warp (lane quarter q).  Per unit it reads the unit's two batches
 // of accumulators back (adding scale * D to the row's NC fp32 sums) and ends
 // tile segments.
-template <int BITS, int G, int NC, int EPI, bool PAIR, class B>
+template <int BITS, int G, int NC, int EPI, bool PAIR, bool CLU, class B>
 __device__ __forceinline__ void epilogue_warp(const Ctx& c, B& bars, uint32_t tmem,
                                               volatile int* abort_flag, int q, int lane,
-                                              int n_units) {
+                                              int n_units, uint32_t fix_smem, uint32_t crank,
+                                              uint32_t csize) {
     using L = Lay<BITS, G, NC>;
     using RM = RowMeta<L::kGPS>;
     const int r = 32 * q + lane;
@@ -994,9 +1053,15 @@ __device__ __forceinline__ void epilogue_warp(const Ctx& c, B& bars, uint32_t tm
         const bool tile_end = cc.i == cc.v.I - 1;
         const bool end = tile_end || cc.last_of_share();
         if (end) {
-            if (!dead)
-                finish_rows<EPI, NC, PAIR>(c, cc.v, acc, cc.t, seg_from_start && tile_end,
-                            seg_from_start && !tile_end, r, q, lane);
+            if (!dead) {
+                if constexpr (CLU)
+                    finish_rows_cluster<EPI, NC>(c, cc.v, acc, cc.t, seg_from_start && tile_end,
+                                                 r, lane, fix_smem, &bars.fix, crank, csize,
+                                                 abort_flag);
+                else
+                    finish_rows<EPI, NC, PAIR>(c, cc.v, acc, cc.t, seg_from_start && tile_end,
+                                               seg_from_start && !tile_end, r, q, lane);
+            }
 #pragma unroll
             for (int j = 0; j < NC; ++j) acc[j] = 0.f;
         }
@@ -1036,7 +1101,9 @@ __device__ __forceinline__ bool wait_deps(const Ctx& c, int upto, int& verified,
 // HOLD: the build can be launched as a programmatic dependent (single
 // projections always; a fused step only in its per-phase launches, a separate
 // build because the fused kernel's speed measured sensitive to any code added).
-template <int BITS, int G, int NC, bool MULTI, int EPI, bool HOLD = !MULTI>
+// CLU: a per-phase build launched in clusters of k CTAs per tile, whose
+// split-K sums travel through rank 0's shared memory (finish_rows_cluster).
+template <int BITS, int G, int NC, bool MULTI, int EPI, bool HOLD = !MULTI, bool CLU = false>
 __global__ void __launch_bounds__(Lay<BITS, G, NC>::kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                    const GemmArgs a, const StepArgs sa) {
@@ -1112,6 +1179,13 @@ __global__ void __launch_bounds__(Lay<BITS, G, NC>::kThreads, 1)
             mbar_init(&bars.dfree[s], L::kEW);
         }
         mbar_init(&bars.drain, 1);
+        if constexpr (CLU) {
+            mbar_init(&bars.fix, 1);
+            // rank 0 expects the sums of the other k - 1 ranks
+            const uint32_t k = cluster_size();
+            if (cluster_rank() == 0 && k > 1)
+                mbar_arrive_expect_tx(&bars.fix, (k - 1) * kBN * NC * 4u);
+        }
         *abort_flag = 0;
         // a dependent launch may place its CTAs on SMs as this grid's CTAs leave
         griddep_launch_dependents();
@@ -1129,6 +1203,13 @@ __global__ void __launch_bounds__(Lay<BITS, G, NC>::kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars.tmem_base;
+    uint32_t crank = 0, csize = 1;
+    if constexpr (CLU) {
+        // every CTA's barriers are initialised before any of them stores into another
+        cluster_sync();
+        crank = cluster_rank();
+        csize = cluster_size();
+    }
 
     const int n_units = bars.n_units;
     constexpr uint32_t kTail = 32 * (L::kUW + L::kEW + 1);  // warps that meet before dealloc
@@ -1398,7 +1479,8 @@ __global__ void __launch_bounds__(Lay<BITS, G, NC>::kThreads, 1)
 
     if (warp >= L::kUW) {
         // ------------------------------------------------------------ epilogue
-        epilogue_warp<BITS, G, NC, EPI, HOLD>(c, bars, tmem, abort_flag, warp & 3, lane, n_units);
+        epilogue_warp<BITS, G, NC, EPI, HOLD, CLU>(c, bars, tmem, abort_flag, warp & 3, lane, n_units,
+                                                   smem_u32 + L::kFixOff, crank, csize);
     } else if constexpr (BITS == 3) {
         // ------------------------------------------------------------ unpack
         static_for<0, L::kSplit>([&](auto hc) {
@@ -1450,9 +1532,55 @@ cudaError_t launch_tc(const CUtensorMap& tmW, const CUtensorMap& tmX, const Gemm
 // wait for one another.  A per-phase launch none of whose projections asks
 // for the activation takes the build without it (measured 3 % faster on the
 // per-phase layer chain; the single fused launch measured faster with it).
+// A per-phase launch in clusters of sa.cluster CTAs (one tile per cluster).
+template <int BITS, int G>
+cudaError_t launch_step_cluster(const StepArgs& sa, cudaStream_t s) {
+    using L = Lay<BITS, G, 16>;
+    if constexpr (!L::kCluOk) {
+        return cudaErrorNotSupported;
+    } else {
+        if (sa.cluster < 2 || sa.cluster > L::kFixMaxK || sa.P % sa.cluster != 0 || sa.act)
+            return cudaErrorInvalidValue;
+        auto kern = gemm_tc_kernel<BITS, G, 16, true, kEpiY, true, true>;
+        cudaError_t e =
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytesClu);
+        if (e != cudaSuccess) return e;
+        CUtensorMap none{};
+        GemmArgs a{};
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3(static_cast<unsigned>(sa.P));
+        cfg.blockDim = dim3(L::kThreads);
+        cfg.dynamicSmemBytes = L::kSmemBytesClu;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[2];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = static_cast<unsigned>(sa.cluster);
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        // whether the device can place clusters of this size at all (checked
+        // once per size; a launch it cannot place is not issued)
+        static int placeable[L::kFixMaxK + 1] = {};  // 0 unknown, 1 yes, 2 no
+        int& ok = placeable[sa.cluster];
+        if (ok == 0) {
+            int n = 0;
+            ok = cudaOccupancyMaxActiveClusters(&n, kern, &cfg) == cudaSuccess && n >= 1 ? 1 : 2;
+            (void)cudaGetLastError();
+        }
+        if (ok != 1) return cudaErrorNotSupported;
+        cfg.numAttrs = sa.pdl ? 2 : 1;
+        return cudaLaunchKernelEx(&cfg, kern, none, none, a, sa);
+    }
+}
+
 template <int BITS, int G, int NC>
 cudaError_t launch_step_nc(const StepArgs& sa, bool cooperative, cudaStream_t s) {
     using L = Lay<BITS, G, NC>;
+    if constexpr (NC == 16)
+        if (sa.cluster > 1) return launch_step_cluster<BITS, G>(sa, s);
     auto kern = !sa.pdl ? gemm_tc_kernel<BITS, G, NC, true, kEpiAny, false>
                 : sa.act ? gemm_tc_kernel<BITS, G, NC, true, kEpiAny, true>
                          : gemm_tc_kernel<BITS, G, NC, true, kEpiY, true>;

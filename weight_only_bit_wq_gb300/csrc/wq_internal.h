@@ -95,6 +95,9 @@ struct StepArgs {
                           // once that kernel completed
     int act;              // with pdl: some projection of the launch asks for the activation
                           // epilogue (otherwise the build without it serves)
+    int cluster;          // > 1: one phase, k = cluster CTAs per tile, each one segment
+                          // (P = k x tiles): launched in clusters of k, split-K sums through
+                          // rank 0's shared memory
 };
 
 // SMs a GEMM grid leaves free.  A launch that is a programmatic dependent of
