@@ -107,6 +107,44 @@ def test_stream_k_schedule_partitions_units(wq, U, P):
     assert wq._lib().wq_internal_schedule_check(U, P) == 0
 
 
+def test_single_projection_grid_rule(wq):
+    # at most SMs - 2 CTAs; where the tiles outnumber them and a divisor of the
+    # tile count lies within 74 % of that budget, whole tiles per CTA
+    g = wq._lib().wq_internal_choose_grid
+    assert g(272, 10, 152) == 136      # 34,816 rows: two whole tiles per CTA
+    assert g(300, 10, 152) == 150      # 150 divides 300
+    assert g(2345, 2, 152) == 150      # no divisor of 2345 in [111, 150]
+    assert g(40, 34, 152) == 150       # fewer tiles than CTAs: the budget
+    assert g(8, 34, 152) == 64         # at most 8 CTAs per tile
+    assert g(3, 1, 152) == 3           # at most one CTA per unit
+    assert g(272, 10, 2) == 1
+
+
+def _phase_grid(wq, T, I, uniform, U, budget=150, nc=16, act=0):
+    P, k = ctypes.c_int(0), ctypes.c_int(0)
+    assert wq._lib().wq_internal_phase_grid(T, I, uniform, U, budget, nc, act, ctypes.byref(P),
+                                            ctypes.byref(k)) == 0
+    return P.value, k.value
+
+
+def test_phase_grid_rule(wq):
+    # the decode layer's phases on a 150-CTA budget
+    assert _phase_grid(wq, 56, 10, 1, 560) == (112, 2)    # q, k, v: two CTAs per tile, clustered
+    assert _phase_grid(wq, 40, 10, 1, 400) == (120, 3)    # o: three per tile
+    assert _phase_grid(wq, 272, 10, 1, 2720) == (136, 0)  # gate/up: two whole tiles per CTA
+    assert _phase_grid(wq, 40, 34, 1, 1360) == (120, 3)   # down
+    # no cluster where a rank would get no unit, for the 32-row build, with the
+    # activation epilogue, or with unequal tiles (then no alignment either)
+    assert _phase_grid(wq, 40, 2, 1, 80) == (80, 2)
+    assert _phase_grid(wq, 40, 1, 1, 40) == (40, 0)
+    assert _phase_grid(wq, 40, 10, 1, 400, nc=32) == (120, 0)
+    assert _phase_grid(wq, 40, 10, 1, 400, act=1) == (120, 0)
+    assert _phase_grid(wq, 56, 10, 0, 500) == (150, 0)
+    # no k CTAs per tile within 74 % of the budget
+    assert _phase_grid(wq, 100, 10, 1, 1000) == (150, 0)
+    assert _phase_grid(wq, 8, 34, 1, 272) == (144, 0)     # 18 CTAs per tile: no cluster
+
+
 def test_gemm_rejects_misaligned_operands(wq):
     # x and wq feed TMA boxes: both 16-byte aligned; bf16 scales 2-byte aligned
     lib = wq._lib()

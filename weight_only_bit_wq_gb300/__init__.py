@@ -90,6 +90,8 @@ def _lib() -> ctypes.CDLL:
             "wq_step_graph_launch": ([P, P], I),
             "wq_step_graph_destroy": ([P], None),
             "wq_internal_schedule_check": ([ctypes.c_longlong, I], I),
+            "wq_internal_choose_grid": ([I, I, I], I),
+            "wq_internal_phase_grid": ([I, I, I, ctypes.c_longlong, I, I, I, P, P], I),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name, None)

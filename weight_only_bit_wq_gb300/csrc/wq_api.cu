@@ -435,6 +435,9 @@ wq_status_t wq_check_workspace(void* workspace, void* stream) {
     return WQ_ERR_TIMEOUT;
 }
 
+// Host-only view of the single-projection grid rule (used by the CPU tests).
+int wq_internal_choose_grid(int T, int I, int sm_count) { return wq::choose_grid(T, I, sm_count); }
+
 // Host-only self check of the stream-K schedule (used by the CPU tests):
 // returns 0 when every unit of [0, U) belongs to exactly one CTA and the
 // closed-form owner of each unit matches the ranges.

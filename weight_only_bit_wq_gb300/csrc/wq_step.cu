@@ -230,6 +230,24 @@ wq_status_t launch_run(const Run& r, Tables tab, int nphase, long long units, bo
 #define WQ_CLUSTER_FIXUP 1
 #endif
 
+// Grid of a per-phase launch over T tiles of I units each (uniform_i: every
+// projection of the phase has I units per tile) and U units in all: shares on
+// tile boundaries where such a grid lies near the budget, and, where that
+// gives each tile k = 2..4 CTAs of one segment each, one cluster per tile.
+struct PhaseGrid {
+    int P, cluster;
+};
+PhaseGrid phase_grid(int T, int I, bool uniform_i, long long U, int budget, int nc, bool act) {
+    PhaseGrid g{};
+    const int Pa = uniform_i ? wq::aligned_grid(T, budget, true) : budget;
+    g.P = static_cast<int>(std::min<long long>(Pa, U));
+    const int k = T > 0 ? g.P / T : 0;
+    if (WQ_CLUSTER_FIXUP && uniform_i && k >= 2 && k <= 4 && k * T == g.P && I >= k &&
+        nc == 16 && !act)
+        g.cluster = k;
+    return g;
+}
+
 wq_status_t launch_phases(const wq_proj_desc_t* projs, const Run& r, Tables tab,
                           const std::vector<wq::PhaseDev>& phases, const std::vector<int>& first,
                           const std::vector<wq::ProjDev>& host, uint8_t* ws,
@@ -260,15 +278,10 @@ wq_status_t launch_phases(const wq_proj_desc_t* projs, const Run& r, Tables tab,
             if (I < 0) I = d.I;
             else if (d.I != I) uniform_i = false;
         }
-        const int budget = wq::gemm_sm_budget(sms);
-        const int Pa = uniform_i ? wq::aligned_grid(T, budget, true) : budget;
-        sa.P = static_cast<int>(std::min<long long>(Pa, phases[p].U));
-        // k CTAs per tile, each one segment: one cluster per tile, the split-K
-        // sums through shared memory
-        const int k = T > 0 ? sa.P / T : 0;
-        if (WQ_CLUSTER_FIXUP && uniform_i && k >= 2 && k <= 4 && k * T == sa.P && I >= k &&
-            r.nc == 16 && !act)
-            sa.cluster = k;
+        const PhaseGrid pg =
+            phase_grid(T, I, uniform_i, phases[p].U, wq::gemm_sm_budget(sms), r.nc, act);
+        sa.P = pg.P;
+        sa.cluster = pg.cluster;
         sa.pdl = prev_kernel ? 1 : 0;
         sa.act = act ? 1 : 0;
         cudaError_t e = cudaSuccess;
@@ -532,3 +545,13 @@ wq_status_t wq_internal_step_stall_probe(const wq_proj_desc_t* projs, int count,
 }
 
 }  // extern "C"
+
+// Host-only view of the per-phase grid rule (used by the CPU tests).
+extern "C" int wq_internal_phase_grid(int T, int I, int uniform_i, long long U, int budget, int nc,
+                                      int act, int* P, int* cluster) {
+    if (!P || !cluster || T <= 0 || U <= 0 || budget <= 0) return 1;
+    const PhaseGrid g = phase_grid(T, I, uniform_i != 0, U, budget, nc, act != 0);
+    *P = g.P;
+    *cluster = g.cluster;
+    return 0;
+}
