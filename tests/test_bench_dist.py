@@ -76,3 +76,14 @@ def test_headline_mode_is_the_faster_chain_mode():
     cfg = bench._config(16, 64, 1, "sequential", 384)
     assert cfg["launches_per_step"] == 384 and "sequential" in cfg["headline"]
     assert bench._config(16, 64, 1)["launches_per_step"] == 1
+
+
+def test_e2e_chunks_cover_the_layers():
+    import bench
+    assert bench.e2e_chunks(64, "8") == [8] * 8
+    assert bench.e2e_chunks(64, "2,6,8,8,8,8,8,8,6,2") == [2, 6] + [8] * 6 + [6, 2]
+    assert bench.e2e_chunks(6, "4") == [4, 2]
+    assert bench.e2e_chunks(64, "taper") == [2, 6] + [8] * 6 + [6, 2]
+    assert bench.e2e_chunks(2, "taper") == [2]
+    with pytest.raises(ValueError):
+        bench.e2e_chunks(64, "8,8")
