@@ -139,18 +139,21 @@ def _chain_outputs(wq, projs, M, flags, ws=None):
     return [d["y"][:M].cpu().numpy() for p, w, x, d in projs], ws
 
 
-def test_phased_cluster_fixup_matches_oracle():
+@pytest.mark.parametrize("fmt", [(4, 128), (3, 128), (2, 64), (4, 32)], ids=lambda f: f"b{f[0]}g{f[1]}")
+def test_phased_cluster_fixup_matches_oracle(fmt):
     # Per-phase launches whose grid gives each tile k = 2..4 CTAs (here 40- and
     # 56-tile projections on a 150-CTA budget: k = 3 and 2) run as one cluster
-    # per tile and add the split-K sums through shared memory.  A chain of one
-    # projection per phase, against the oracle, bitwise across repeats and
-    # across row counts.
+    # per tile and add the split-K sums through shared memory (formats whose
+    # build has no room for the cluster buffer take the global-memory path).
+    # A chain of one projection per phase, against the oracle, bitwise across
+    # repeats and across row counts.
     import weight_only_bit_wq_gb300 as wq
+    bits, G = fmt
     shapes = [(2048, 5120), (5120, 5120), (1536, 7168), (17408, 5120)]  # (K, N)
     M = 5
     projs = []
     for i, (K, N) in enumerate(shapes):
-        p = synth.Projection(f"c{i}", M, N, K, 4, 128, 500, index=i)
+        p = synth.Projection(f"c{i}", M, N, K, bits, G, 500, index=i)
         w, x, d = to_dev_host_inputs(p)
         d["y"] = torch.empty((M, N), dtype=torch.float32, device=dev())
         projs.append((p, w, x, d))
