@@ -269,8 +269,8 @@ typedef struct wq_proj_desc {
  * grid whose shares fall on tile boundaries where one lies near the SM count,
  * so its split can differ from WQ_STEP_FUSED's: results agree with the fused
  * launch to rounding; a row alone is still bit-identical to the same row
- * stacked, and repeated steps are bit-identical.  A launch with 2 to 4 CTAs
- * per tile runs one thread-block cluster per tile, whose split-K sums meet in
+ * stacked, and repeated steps are bit-identical.  A launch with two CTAs per
+ * tile runs one thread-block cluster per tile, whose split-K sums meet in
  * shared memory instead of global memory.  Not part of the pages: a launch
  * plan for the same step. */
 #define WQ_STEP_PHASES 2u

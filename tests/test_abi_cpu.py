@@ -130,15 +130,15 @@ def _phase_grid(wq, T, I, uniform, U, budget=150, nc=16, act=0):
 def test_phase_grid_rule(wq):
     # the decode layer's phases on a 150-CTA budget
     assert _phase_grid(wq, 56, 10, 1, 560) == (112, 2)    # q, k, v: two CTAs per tile, clustered
-    assert _phase_grid(wq, 40, 10, 1, 400) == (120, 3)    # o: three per tile
+    assert _phase_grid(wq, 40, 10, 1, 400) == (120, 0)    # o: three per tile, not clustered
     assert _phase_grid(wq, 272, 10, 1, 2720) == (136, 0)  # gate/up: two whole tiles per CTA
-    assert _phase_grid(wq, 40, 34, 1, 1360) == (120, 3)   # down
+    assert _phase_grid(wq, 40, 34, 1, 1360) == (120, 0)   # down
     # no cluster where a rank would get no unit, for the 32-row build, with the
     # activation epilogue, or with unequal tiles (then no alignment either)
     assert _phase_grid(wq, 40, 2, 1, 80) == (80, 2)
     assert _phase_grid(wq, 40, 1, 1, 40) == (40, 0)
-    assert _phase_grid(wq, 40, 10, 1, 400, nc=32) == (120, 0)
-    assert _phase_grid(wq, 40, 10, 1, 400, act=1) == (120, 0)
+    assert _phase_grid(wq, 56, 10, 1, 560, nc=32) == (112, 0)
+    assert _phase_grid(wq, 56, 10, 1, 560, act=1) == (112, 0)
     assert _phase_grid(wq, 56, 10, 0, 500) == (150, 0)
     # no k CTAs per tile within 74 % of the budget
     assert _phase_grid(wq, 100, 10, 1, 1000) == (150, 0)

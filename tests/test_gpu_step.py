@@ -141,10 +141,11 @@ def _chain_outputs(wq, projs, M, flags, ws=None):
 
 @pytest.mark.parametrize("fmt", [(4, 128), (3, 128), (2, 64), (4, 32)], ids=lambda f: f"b{f[0]}g{f[1]}")
 def test_phased_cluster_fixup_matches_oracle(fmt):
-    # Per-phase launches whose grid gives each tile k = 2..4 CTAs (here 40- and
-    # 56-tile projections on a 150-CTA budget: k = 3 and 2) run as one cluster
-    # per tile and add the split-K sums through shared memory (formats whose
-    # build has no room for the cluster buffer take the global-memory path).
+    # Per-phase launches whose grid gives each tile two CTAs (here the 56-tile
+    # projection on a 150-CTA budget) run as one cluster per tile and add the
+    # split-K sums through shared memory (formats whose build has no room for
+    # the cluster buffer, and the 40-tile projections with three CTAs per
+    # tile, take the global-memory path).
     # A chain of one projection per phase, against the oracle, bitwise across
     # repeats and across row counts.
     import weight_only_bit_wq_gb300 as wq

@@ -221,11 +221,8 @@ wq_status_t launch_run(const Run& r, Tables tab, int nphase, long long units, bo
 
 // One launch per phase of a run (tables from to_phase_tables); every launch
 // that follows another kernel of the step is a programmatic dependent one.
-// Per-phase launches with k = 2..4 CTAs per tile run one cluster per tile
-// (split-K sums through shared memory).  Measured on the 64-layer chain's
-// 8-layer copy: 0.546 against 0.549 ms; clusters start later than single
-// CTAs (a cluster needs k free SMs of one GPC), which takes back most of
-// what the shorter fix-up saves.
+// Per-phase launches with two CTAs per tile run one cluster per tile
+// (split-K sums through shared memory); see phase_grid.
 #ifndef WQ_CLUSTER_FIXUP
 #define WQ_CLUSTER_FIXUP 1
 #endif
@@ -233,7 +230,11 @@ wq_status_t launch_run(const Run& r, Tables tab, int nphase, long long units, bo
 // Grid of a per-phase launch over T tiles of I units each (uniform_i: every
 // projection of the phase has I units per tile) and U units in all: shares on
 // tile boundaries where such a grid lies near the budget, and, where that
-// gives each tile k = 2..4 CTAs of one segment each, one cluster per tile.
+// gives each tile two CTAs of one segment each, one cluster (pair) per tile.
+// Clusters of three measured slower: a cluster needs all its SMs free in one
+// GPC as the previous launch drains, and triples are placed later than
+// pairs (8-layer chain: pairs only 0.538 ms, pairs and triples 0.543, triples
+// only 0.585, none 0.547).
 struct PhaseGrid {
     int P, cluster;
 };
@@ -242,8 +243,7 @@ PhaseGrid phase_grid(int T, int I, bool uniform_i, long long U, int budget, int 
     const int Pa = uniform_i ? wq::aligned_grid(T, budget, true) : budget;
     g.P = static_cast<int>(std::min<long long>(Pa, U));
     const int k = T > 0 ? g.P / T : 0;
-    if (WQ_CLUSTER_FIXUP && uniform_i && k >= 2 && k <= 4 && k * T == g.P && I >= k &&
-        nc == 16 && !act)
+    if (WQ_CLUSTER_FIXUP && uniform_i && k == 2 && k * T == g.P && I >= k && nc == 16 && !act)
         g.cluster = k;
     return g;
 }
